@@ -1,0 +1,199 @@
+/*
+ * mla_dcp.h -- C ABI of the GB300 (sm_103a) decode-step MLA library.
+ *
+ * One decode step of Multi-head Latent Attention over a paged, compressed
+ * latent KV cache whose history is split into context shards:
+ *
+ *   mla_dcp_decode_partial  per-shard (and CURRENT-chunk) partial attention
+ *                           outputs and their log-sum-exp
+ *   mla_lse_combine         LSE-weighted merge of the partials: the result
+ *                           equals one softmax over the whole sequence
+ *   mla_vup                 per-head V up-projection, latent 512 -> 128
+ *   mla_lse_combine_vup     the combine with the V-up fused into its epilogue
+ *   mla_gather_kv           test hook: bit-exact gather of paged history
+ *
+ * Sources (web pages, cited by title and section):
+ *   [PR]  vllm-ascend PR #16977 study page, "DCP decode: streams and V-up"
+ *         (huashanblogllm.xyz study-dcp-decode-streams-vup)
+ *   [TP]  MLA multi-GPU TP configuration article (hncyxsy.com news 238223)
+ *   [K3]  "RTPLLM推理优化：K3芯片上MLA注意力的DCP与通算融合实践" (zwxr.cn 254603)
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library allocates no device memory in any of these calls.
+ *   - Tensors are dense, C-contiguous, in the layouts stated per argument.
+ *     Every base pointer must be 16-byte aligned.
+ *   - Every call is asynchronous on `stream` (NULL = legacy default stream)
+ *     and never synchronises the host.
+ *   - Return value: MLA_OK (0) or an mla_status code for errors the host can
+ *     see (null pointer, bad size, bad dtype, misalignment, launch failure).
+ *     Nothing is launched when a host check fails.
+ *   - Errors only the device can see (a block_table entry outside
+ *     [0, num_blocks), a pipeline wait that ran out of its spin budget) are
+ *     written to *err_flag (a caller-owned device int32, may be NULL) with
+ *     the first writer winning; read it after synchronising.  When it is
+ *     non-zero the outputs of that call are unspecified.  No kernel traps or
+ *     spins without bound.
+ */
+#ifndef MLA_DCP_H
+#define MLA_DCP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* mla_stream_t;
+
+/* Element types.  Q, the cache, kv_cur and W_UV share one storage dtype
+ * (BF16 or FP16); partial outputs may also be FP32. */
+typedef enum { MLA_BF16 = 0, MLA_FP16 = 1, MLA_FP32 = 2 } mla_dtype;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_NULL_POINTER = 1,  /* a required pointer is NULL                   */
+  MLA_ERR_BAD_SHAPE = 2,     /* a size is out of range or inconsistent       */
+  MLA_ERR_BAD_DTYPE = 3,     /* dtype not supported for this argument        */
+  MLA_ERR_MISALIGNED = 4,    /* a base pointer is not 16-byte aligned        */
+  MLA_ERR_BAD_SHARDS = 5,    /* num_shards / num_parts out of range          */
+  MLA_ERR_BAD_BLOCK = 6,     /* block_size unsupported                       */
+  MLA_ERR_CUDA = 7,          /* a CUDA runtime/driver call failed            */
+} mla_status;
+
+/* Device error codes written to *err_flag. */
+enum { MLA_DEV_OK = 0, MLA_DEV_BAD_BLOCK_ID = 1, MLA_DEV_WAIT_TIMEOUT = 2 };
+
+enum {
+  MLA_D_LATENT = 512, /* kv_lora_rank: width of c_KV  ([TP] "物理矛盾")          */
+  MLA_D_ROPE = 64,    /* width of the decoupled RoPE key k_R ([TP] "物理矛盾")   */
+  MLA_D_QK = 576,     /* values per cached token ([TP] route A, ~1.15 KB/token) */
+  MLA_D_V = 128,      /* per-head V width after the up-projection ([PR] block A) */
+  MLA_MAX_HEADS = 128,
+  MLA_MAX_SHARDS = 64
+};
+
+/*
+ * mla_dcp_decode_partial -- partial attention per context shard.
+ *
+ * Defines: [PR] glossary "DCP" and "LSE", and the HISTORY / CURRENT split of
+ * the decode step (the section on the two-segment decode step; code blocks B and C):
+ * the history KV is split along the sequence into `num_shards` shards, each
+ * shard yields a partial output and its LSE; the CURRENT chunk is attended
+ * with a causal window mask and yields one more partial.
+ *
+ * For sequence b, query token i, head h and part p:
+ *   s_t   = scale * (q_abs[b,i,h,:] . c_t + q_pe[b,i,h,:] . kR_t)
+ *   o_part[b,i,p,h,:] = sum_t softmax_t(s) * c_t   over the part's tokens
+ *   lse_part[b,i,p,h] = ln sum_t exp(s_t)          (natural log)
+ * where c_t = cache entry [0:512) and kR_t = [512:576).  History token t of
+ * sequence b is kv_cache[block_table[b][t / block_size]][t % block_size].
+ * Shard s (0 <= s < num_shards) covers history tokens
+ *   [s*len, min(L_b, (s+1)*len)),  len = block_size * ceil(L_b / (num_shards*block_size)),
+ * L_b = seq_lens[b].  History is fully visible to every query token.
+ * If kv_cur != NULL, part p = num_shards is the CURRENT segment: query token
+ * i sees kv_cur[b, j] for j <= i.
+ * A part with no visible token gets o = 0 and lse = -inf.
+ *
+ * Arguments
+ *   q_abs      [B, q_len, H, 512] in_dtype  query absorbed into latent space
+ *   q_pe       [B, q_len, H, 64]  in_dtype  RoPE query, already rotated
+ *   kv_cache   [num_blocks, block_size, 576] in_dtype
+ *   block_table[B, max_blocks] int32   physical block ids; entries past
+ *              ceil(L_b / block_size) are never read
+ *   seq_lens   [B] int32 (device)  history lengths, 0 <= L_b <= max_blocks*block_size
+ *   kv_cur     [B, q_len, 576] in_dtype, or NULL (no CURRENT segment)
+ *   B >= 1; 1 <= q_len <= 8; 1 <= H <= 128; block_size in {16,32,64,128,256};
+ *   1 <= num_shards <= 64; scale > 0 (1/sqrt(192) for the 128+64 head width)
+ *   in_dtype   MLA_BF16 or MLA_FP16;  part_dtype MLA_BF16, MLA_FP16 or MLA_FP32
+ *   o_part     [B, q_len, P, H, 512] part_dtype, P = num_shards + (kv_cur != NULL)
+ *   lse_part   [B, q_len, P, H] float32
+ *   err_flag   device int32 or NULL (see conventions)
+ * Returns MLA_OK or an mla_status.
+ */
+int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_cache,
+                           const int32_t* block_table, const int32_t* seq_lens,
+                           const void* kv_cur, int B, int q_len, int H, int num_blocks,
+                           int block_size, int max_blocks, int num_shards, float scale,
+                           int in_dtype, int part_dtype, void* o_part, float* lse_part,
+                           int32_t* err_flag, mla_stream_t stream);
+
+/*
+ * mla_lse_combine -- merge partials by their log-sum-exps.
+ *
+ * Defines: [PR] glossary "LSE" and the fourth change (combine without packing the
+ * current partial): all history shards plus the local CURRENT partial are merged
+ * exactly once; the local partial is read in place (local_output /
+ * local_lse) instead of being packed with the others; partials of any of
+ * BF16 / FP16 / FP32 are read directly with no FP32 copy ([PR] first change,
+ * dtype pass-through).
+ *   LSE = ln sum_p exp(lse_p);   o = sum_p exp(lse_p - LSE) * o_p
+ * Parts with lse = -inf carry zero weight; if every part is empty, o = 0 and
+ * LSE = -inf.  Parts are visited in index order 0..num_parts-1, then local.
+ *
+ *   o_part    [T, num_parts, H, 512] part_dtype  (T = B * q_len)
+ *   lse_part  [T, num_parts, H] float32
+ *   o_local   [T, H, 512] part_dtype or NULL;  lse_local [T, H] float32 or NULL
+ *             (both NULL or both set)
+ *   T >= 1; 1 <= H <= 128; 1 <= num_parts (+1 if local) <= 65
+ *   o_latent  [T, H, 512] out_dtype (MLA_BF16 / MLA_FP16 / MLA_FP32)
+ *   lse_out   [T, H] float32, or NULL
+ */
+int mla_lse_combine(const void* o_part, const float* lse_part, int num_parts,
+                    const void* o_local, const float* lse_local, int T, int H, int part_dtype,
+                    int out_dtype, void* o_latent, float* lse_out, mla_stream_t stream);
+
+/*
+ * mla_vup -- batch-major V up-projection.
+ *
+ * Defines: [PR] code block A (_v_up_proj_batch_major): the latent output is
+ * viewed as [T, H, 512], each head is multiplied by W_UV[h] (512 x 128), and
+ * the result is returned as [T, H*128] with no transposes in memory.
+ *   out[t, h*128 + v] = sum_k o_latent[t, h, k] * W_UV[h, k, v]
+ *
+ *   o_latent [T, H, 512] dtype;  W_UV [H, 512, 128] dtype
+ *   dtype MLA_BF16 or MLA_FP16 (one dtype for both operands; fp32 accumulate)
+ *   out      [T, H*128] dtype
+ *   1 <= T <= 65536; 1 <= H <= 128;  err_flag as above (may be NULL)
+ */
+int mla_vup(const void* o_latent, const void* W_UV, int T, int H, int dtype, void* out,
+            int32_t* err_flag, mla_stream_t stream);
+
+/*
+ * mla_lse_combine_vup -- mla_lse_combine and mla_vup in one launch.  The
+ * combined latent of each head is rounded to `dtype` and fed straight to the
+ * up-projection from on-chip memory.  Arguments as in the two calls above;
+ * o_latent (written too, if non-NULL) and out use `dtype`.
+ *   1 <= T <= 65536 (rows are processed in tiles of 64)
+ */
+int mla_lse_combine_vup(const void* o_part, const float* lse_part, int num_parts,
+                        const void* o_local, const float* lse_local, const void* W_UV, int T,
+                        int H, int part_dtype, int dtype, void* out, void* o_latent,
+                        float* lse_out, int32_t* err_flag, mla_stream_t stream);
+
+/*
+ * mla_gather_kv -- test hook: copy each sequence's paged history into a
+ * dense buffer, bit-exactly ([PR] code block B: the HISTORY call reads the
+ * cache through block_table / block_size / cp_history_seq_len).
+ *   dst[b, t, :] = kv_cache[block_table[b][t / block_size]][t % block_size][:]
+ *   for t < seq_lens[b]; rows t >= seq_lens[b] (up to max_len) are zeroed.
+ *   elem_bytes 2 (bf16 / fp16); dst [B, max_len, 576] elements.
+ *   A block id outside [0, num_blocks) sets MLA_DEV_BAD_BLOCK_ID and its
+ *   rows are zeroed.
+ */
+int mla_gather_kv(const void* kv_cache, const int32_t* block_table, const int32_t* seq_lens,
+                  int B, int num_blocks, int block_size, int max_blocks, int max_len,
+                  void* dst, int32_t* err_flag, mla_stream_t stream);
+
+/* Human-readable text of an mla_status or device error code. */
+const char* mla_get_error_string(int status);
+const char* mla_device_error_string(int code);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_DCP_H */

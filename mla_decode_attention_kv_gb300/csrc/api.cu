@@ -1,0 +1,219 @@
+// C ABI of the library (declared in include/mla_dcp.h): host-side argument
+// checks, TMA tensor-map encoding and kernel launches.  No call allocates
+// device memory or synchronises the host.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include "../../include/mla_dcp.h"
+#include "kernels.cuh"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a row-major [rows, cols] 16-bit tensor, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+              uint32_t box_cols, uint32_t box_rows, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool is_half_dtype(int d) { return d == MLA_BF16 || d == MLA_FP16; }
+bool is_part_dtype(int d) { return d == MLA_BF16 || d == MLA_FP16 || d == MLA_FP32; }
+
+int launched(int rc) {
+  if (rc != 0) return MLA_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_version(void) { return 100; }
+
+const char* mla_get_error_string(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case MLA_ERR_BAD_SHAPE: return "a size is out of range or inconsistent";
+    case MLA_ERR_BAD_DTYPE: return "dtype not supported for this argument";
+    case MLA_ERR_MISALIGNED: return "a base pointer is not 16-byte aligned";
+    case MLA_ERR_BAD_SHARDS: return "num_shards / num_parts out of range";
+    case MLA_ERR_BAD_BLOCK: return "block_size unsupported";
+    case MLA_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    default: return "unknown status";
+  }
+}
+
+const char* mla_device_error_string(int code) {
+  switch (code) {
+    case MLA_DEV_OK: return "ok";
+    case MLA_DEV_BAD_BLOCK_ID: return "block_table entry outside [0, num_blocks)";
+    case MLA_DEV_WAIT_TIMEOUT: return "a pipeline wait exceeded its spin budget";
+    default: return "unknown device error";
+  }
+}
+
+int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_cache,
+                           const int32_t* block_table, const int32_t* seq_lens,
+                           const void* kv_cur, int B, int q_len, int H, int num_blocks,
+                           int block_size, int max_blocks, int num_shards, float scale,
+                           int in_dtype, int part_dtype, void* o_part, float* lse_part,
+                           int32_t* err_flag, mla_stream_t stream) {
+  if (!q_abs || !q_pe || !kv_cache || !block_table || !seq_lens || !o_part || !lse_part)
+    return MLA_ERR_NULL_POINTER;
+  if (!is_half_dtype(in_dtype) || !is_part_dtype(part_dtype)) return MLA_ERR_BAD_DTYPE;
+  if (B < 1 || q_len < 1 || q_len > 8 || H < 1 || H > MLA_MAX_HEADS || num_blocks < 1 ||
+      max_blocks < 1 || !(scale > 0.f) || !std::isfinite(scale))
+    return MLA_ERR_BAD_SHAPE;
+  if (num_shards < 1 || num_shards > MLA_MAX_SHARDS) return MLA_ERR_BAD_SHARDS;
+  if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128 &&
+      block_size != 256)
+    return MLA_ERR_BAD_BLOCK;
+  if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX ||
+      static_cast<int64_t>(B) * q_len * H > INT32_MAX / 2)
+    return MLA_ERR_BAD_SHAPE;
+  if (!aligned16(q_abs) || !aligned16(q_pe) || !aligned16(kv_cache) || !aligned16(o_part) ||
+      (kv_cur && !aligned16(kv_cur)) || !aligned16(lse_part))
+    return MLA_ERR_MISALIGNED;
+
+  const bool bf16 = in_dtype == MLA_BF16;
+  const int box_rows = block_size < mla::kPartialTile ? block_size : mla::kPartialTile;
+  const uint64_t qrows = static_cast<uint64_t>(B) * q_len * H;
+  CUtensorMap tm_qabs, tm_qpe, tm_kv, tm_cur;
+  if (!make_map(&tm_qabs, q_abs, 512, qrows, 1024, 64, 128, bf16) ||
+      !make_map(&tm_qpe, q_pe, 64, qrows, 128, 64, 128, bf16) ||
+      !make_map(&tm_kv, kv_cache, 576, static_cast<uint64_t>(num_blocks) * block_size, 1152, 64,
+                box_rows, bf16))
+    return MLA_ERR_CUDA;
+  if (kv_cur) {
+    if (!make_map(&tm_cur, kv_cur, 576, static_cast<uint64_t>(B) * q_len, 1152, 64, box_rows,
+                  bf16))
+      return MLA_ERR_CUDA;
+  } else {
+    tm_cur = tm_kv;   // never read
+  }
+
+  mla::PartialParams pp;
+  pp.block_table = block_table;
+  pp.seq_lens = seq_lens;
+  pp.o_part = o_part;
+  pp.lse_part = lse_part;
+  pp.err = err_flag;
+  pp.B = B;
+  pp.q_len = q_len;
+  pp.H = H;
+  pp.num_blocks = num_blocks;
+  pp.bs = block_size;
+  pp.max_blocks = max_blocks;
+  pp.S = num_shards;
+  pp.has_cur = kv_cur ? 1 : 0;
+  pp.P = num_shards + pp.has_cur;
+  const int64_t units = static_cast<int64_t>(B) * q_len * pp.P;
+  if (units > INT32_MAX) return MLA_ERR_BAD_SHAPE;
+  pp.num_units = static_cast<int>(units);
+  pp.box_rows = box_rows;
+  pp.scale_log2 = scale * 1.4426950408889634f;
+  pp.part_dtype = part_dtype;
+  return launched(mla::launch_partial(tm_qabs, tm_qpe, tm_kv, tm_cur, pp, bf16,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mla_lse_combine(const void* o_part, const float* lse_part, int num_parts, const void* o_local,
+                    const float* lse_local, int T, int H, int part_dtype, int out_dtype,
+                    void* o_latent, float* lse_out, mla_stream_t stream) {
+  if (!o_part || !lse_part || !o_latent) return MLA_ERR_NULL_POINTER;
+  if ((o_local == nullptr) != (lse_local == nullptr)) return MLA_ERR_NULL_POINTER;
+  if (!is_part_dtype(part_dtype) || !is_part_dtype(out_dtype)) return MLA_ERR_BAD_DTYPE;
+  if (T < 1 || H < 1 || H > MLA_MAX_HEADS) return MLA_ERR_BAD_SHAPE;
+  if (num_parts < 1 || num_parts > MLA_MAX_SHARDS + 1) return MLA_ERR_BAD_SHARDS;
+  if (!aligned16(o_part) || !aligned16(o_latent) || (o_local && !aligned16(o_local)))
+    return MLA_ERR_MISALIGNED;
+  return launched(mla::launch_combine(o_part, lse_part, num_parts, o_local, lse_local, T, H,
+                                      part_dtype, out_dtype, o_latent, lse_out,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static int vup_common(bool combine, const void* o_part, const float* lse_part, int num_parts,
+                      const void* o_local, const float* lse_local, const void* o_latent_in,
+                      const void* W_UV, int T, int H, int part_dtype, int dtype, void* out,
+                      void* o_latent_out, float* lse_out, int32_t* err_flag,
+                      mla_stream_t stream) {
+  if (!W_UV || !out) return MLA_ERR_NULL_POINTER;
+  if (!is_half_dtype(dtype)) return MLA_ERR_BAD_DTYPE;
+  if (T < 1 || T > 65536 || H < 1 || H > MLA_MAX_HEADS) return MLA_ERR_BAD_SHAPE;
+  if (!aligned16(W_UV) || !aligned16(out)) return MLA_ERR_MISALIGNED;
+  const bool bf16 = dtype == MLA_BF16;
+  CUtensorMap tm_w;
+  if (!make_map(&tm_w, W_UV, 128, static_cast<uint64_t>(H) * 512, 256, 64, 256, bf16))
+    return MLA_ERR_CUDA;
+  return launched(mla::launch_vup(tm_w, combine, bf16, o_part, lse_part, num_parts, o_local,
+                                  lse_local, o_latent_in, T, H, part_dtype, out, o_latent_out,
+                                  lse_out, err_flag, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mla_vup(const void* o_latent, const void* W_UV, int T, int H, int dtype, void* out,
+            int32_t* err_flag, mla_stream_t stream) {
+  if (!o_latent) return MLA_ERR_NULL_POINTER;
+  if (!aligned16(o_latent)) return MLA_ERR_MISALIGNED;
+  return vup_common(false, nullptr, nullptr, 0, nullptr, nullptr, o_latent, W_UV, T, H, dtype,
+                    dtype, out, nullptr, nullptr, err_flag, stream);
+}
+
+int mla_lse_combine_vup(const void* o_part, const float* lse_part, int num_parts,
+                        const void* o_local, const float* lse_local, const void* W_UV, int T,
+                        int H, int part_dtype, int dtype, void* out, void* o_latent,
+                        float* lse_out, int32_t* err_flag, mla_stream_t stream) {
+  if (!o_part || !lse_part) return MLA_ERR_NULL_POINTER;
+  if ((o_local == nullptr) != (lse_local == nullptr)) return MLA_ERR_NULL_POINTER;
+  if (!is_part_dtype(part_dtype)) return MLA_ERR_BAD_DTYPE;
+  if (num_parts < 1 || num_parts > MLA_MAX_SHARDS + 1) return MLA_ERR_BAD_SHARDS;
+  if (!aligned16(o_part) || (o_local && !aligned16(o_local)) ||
+      (o_latent && !aligned16(o_latent)))
+    return MLA_ERR_MISALIGNED;
+  return vup_common(true, o_part, lse_part, num_parts, o_local, lse_local, nullptr, W_UV, T, H,
+                    part_dtype, dtype, out, o_latent, lse_out, err_flag, stream);
+}
+
+int mla_gather_kv(const void* kv_cache, const int32_t* block_table, const int32_t* seq_lens, int B,
+                  int num_blocks, int block_size, int max_blocks, int max_len, void* dst,
+                  int32_t* err_flag, mla_stream_t stream) {
+  if (!kv_cache || !block_table || !seq_lens || !dst) return MLA_ERR_NULL_POINTER;
+  if (B < 1 || B > 65535 || num_blocks < 1 || block_size < 1 || max_blocks < 1 || max_len < 1)
+    return MLA_ERR_BAD_SHAPE;
+  if (!aligned16(kv_cache) || !aligned16(dst)) return MLA_ERR_MISALIGNED;
+  return launched(mla::launch_gather(kv_cache, block_table, seq_lens, B, num_blocks, block_size,
+                                     max_blocks, max_len, dst, err_flag,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

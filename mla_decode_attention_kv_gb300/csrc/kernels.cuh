@@ -1,0 +1,40 @@
+// Launchers of the CUDA kernels and the parameter block of the partial
+// kernel, shared by the kernels and the C ABI layer.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace mla {
+
+struct PartialParams {
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  void* o_part;
+  float* lse_part;
+  int* err;
+  int B, q_len, H, num_blocks, bs, max_blocks, S, P, has_cur;
+  int num_units;
+  int box_rows;          // rows per TMA box of the KV maps: min(tile, block_size)
+  float scale_log2;      // softmax scale * log2(e)
+  int part_dtype;        // 0 bf16, 1 fp16, 2 fp32
+};
+
+// Tokens per KV tile of the partial kernel.
+constexpr int kPartialTile = 32;
+
+int launch_partial(const CUtensorMap& qabs, const CUtensorMap& qpe, const CUtensorMap& kv,
+                   const CUtensorMap& cur, const PartialParams& pp, bool bf16,
+                   cudaStream_t stream);
+int launch_combine(const void* o_part, const float* lse_part, int P, const void* o_local,
+                   const float* lse_local, int T, int H, int part_dt, int out_dt, void* o_latent,
+                   float* lse_out, cudaStream_t stream);
+int launch_vup(const CUtensorMap& tm_w, bool combine, bool bf16, const void* o_part,
+               const float* lse_part, int P, const void* o_local, const float* lse_local,
+               const void* o_latent_in, int T, int H, int part_dt, void* out, void* o_latent_out,
+               float* lse_out, int* err, cudaStream_t stream);
+int launch_gather(const void* kv_cache, const int32_t* block_table, const int32_t* seq_lens,
+                  int B, int num_blocks, int bs, int max_blocks, int max_len, void* dst, int* err,
+                  cudaStream_t stream);
+
+}  // namespace mla

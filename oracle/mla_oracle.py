@@ -38,7 +38,7 @@ and the section it falls in:
    window mask (query i sees current tokens 0..i) and produce one more
    partial ([PR] code block C, ``sparse_mode=3``).  History is fully visible.
 6. LSE combine.  Merging the partials by their LSEs equals one softmax over
-   the whole sequence ([PR] section "DCP decode 一步要把注意力拆成两段").
+   the whole sequence ([PR] section describing the two-segment decode step).
    Partials with no visible token (lse = -inf) carry weight zero.
 7. V-up.  The combined output stays batch-major [T, H, 512]; each head is
    multiplied by W_UV[h] (512 x 128) and the result reshaped to [T, H*128]
@@ -91,6 +91,8 @@ def gather_history(kv_cache_bits, block_table_row, block_size: int, L: int):
 def gather_history_fast(kv_cache_bits, block_table_row, block_size, L):
     """Same as ``gather_history`` one block at a time (used at large L)."""
     nb = (L + block_size - 1) // block_size
+    if nb == 0:
+        return np.empty((0, kv_cache_bits.shape[-1]), dtype=kv_cache_bits.dtype)
     pages = kv_cache_bits[np.asarray(block_table_row[:nb], dtype=np.int64)]
     return pages.reshape(nb * block_size, -1)[:L]
 

@@ -1,0 +1,261 @@
+"""CUDA path versus the fp64 oracle, through the C ABI.
+
+Small cases are compared element by element (every shard partial, every
+LSE, the combined latent and the V-up output); the full-size workloads are
+run in the launch configuration the bench times and compared on sampled
+sequences and heads.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mla_decode_attention_kv_gb300 import api, inputs
+from oracle import mla_oracle as om
+
+from gpu_util import DeviceProblem, assert_lse_close, assert_out_close, f64
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    # several 32-token tiles per shard with ragged tails, shuffled pages
+    "ragged_bf16_cur": inputs.DecodeConfig(
+        name="s1", batch=3, heads=128, q_len=1, num_shards=3, block_size=32,
+        ragged=(1, 400), current=True, seed=21),
+    # MTP-like: two query tokens, causal CURRENT chunk, fp16, 64-token pages
+    "mtp_fp16": inputs.DecodeConfig(
+        name="s2", batch=2, heads=128, q_len=2, num_shards=2, block_size=64,
+        history=300, current=True, dtype="fp16", part_dtype="fp16", seed=22),
+    # few heads (padded MMA rows), fp32 partials, 16-token pages
+    "heads16_fp32part": inputs.DecodeConfig(
+        name="s3", batch=2, heads=16, q_len=1, num_shards=4, block_size=16,
+        ragged=(20, 200), dtype="bf16", part_dtype="fp32", seed=23),
+    "tiny": inputs.CONFIGS["tiny"],
+}
+
+
+def _check_partials(dp, o_part, lse_part):
+    ref_o, ref_l = om.decode_partials(dp.prob)
+    got_o, got_l = f64(o_part), f64(lse_part)
+    assert_lse_close(got_l, ref_l, "lse_part")
+    for s in range(ref_o.shape[2]):
+        assert_out_close(got_o[:, :, s], ref_o[:, :, s], f"o_part shard {s}")
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_partials_match_oracle(name):
+    dp = DeviceProblem(inputs.make_problem(SMALL[name]))
+    o_part, lse_part = dp.partial()
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    _check_partials(dp, o_part, lse_part)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_decode_step_matches_oracle(name):
+    dp = DeviceProblem(inputs.make_problem(SMALL[name]))
+    H = dp.prob.cfg.heads
+    o_latent = torch.empty((dp.prob.cfg.batch * dp.prob.cfg.q_len, H, 512), dtype=dp.dt,
+                           device=dp.dev)
+    lse = torch.empty((dp.prob.cfg.batch * dp.prob.cfg.q_len, H), dtype=torch.float32,
+                      device=dp.dev)
+    o_part, lse_part = dp.partial()
+    out = api.mla_lse_combine_vup(o_part, lse_part, dp.W, o_latent=o_latent, lse_out=lse,
+                                  err_flag=dp.err)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    ref_o, ref_l, ref_out = om.decode_reference(dp.prob)
+    B, q = dp.prob.cfg.batch, dp.prob.cfg.q_len
+    assert_out_close(f64(o_latent).reshape(B, q, H, 512), ref_o, "o_latent")
+    assert_lse_close(f64(lse).reshape(B, q, H), ref_l, "lse")
+    assert_out_close(f64(out), ref_out, "out")
+
+
+@pytest.mark.parametrize("part", ["bf16", "fp16", "fp32"])
+@pytest.mark.parametrize("local", [False, True])
+def test_combine_dtypes_and_local(part, local):
+    """Combine alone on oracle partials rounded to each partial dtype (the
+    BF16 / FP16 / FP32 history-output parametrisation), with and without
+    the CURRENT partial passed separately."""
+    cfg = inputs.DecodeConfig(name="c", batch=2, heads=128, q_len=2, num_shards=5,
+                              block_size=32, ragged=(1, 300), current=True, seed=31)
+    prob = inputs.make_problem(cfg, seq_lens=[0, 270])      # sequence 0: all shards empty
+    ref_o, ref_l = om.decode_partials(prob)
+    dev = torch.device("cuda:0")
+    pdt = api.torch_dtype(part)
+    o_part = torch.tensor(ref_o, dtype=torch.float32).to(pdt).to(dev)
+    lse_part = torch.tensor(ref_l, dtype=torch.float32).to(dev)
+    T = cfg.batch * cfg.q_len
+    if local:
+        S = cfg.num_shards
+        o_hist = o_part[:, :, :S].contiguous()
+        l_hist = lse_part[:, :, :S].contiguous()
+        o_loc = o_part[:, :, S].contiguous()
+        l_loc = lse_part[:, :, S].contiguous()
+        got_o, got_l = api.mla_lse_combine(o_hist, l_hist, o_local=o_loc, lse_local=l_loc,
+                                           out_dtype=torch.float32)
+    else:
+        got_o, got_l = api.mla_lse_combine(o_part, lse_part, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    exp_o, exp_l = om.lse_combine(f64(o_part.float()), ref_l)
+    assert_out_close(f64(got_o).reshape(exp_o.shape), exp_o, "o")
+    assert_lse_close(f64(got_l).reshape(exp_l.shape), exp_l, "lse")
+    assert got_o.shape == (T, cfg.heads, 512)
+
+
+def test_vup_matches_oracle():
+    rng = np.random.default_rng(5)
+    for T, H in ((1, 1), (37, 8), (130, 128)):
+        o = rng.standard_normal((T, H, 512)).astype(np.float32)
+        W = (rng.standard_normal((H, 512, 128)) * 0.05).astype(np.float32)
+        o_t = torch.tensor(o).to(torch.bfloat16).cuda()
+        W_t = torch.tensor(W).to(torch.bfloat16).cuda()
+        out = api.mla_vup(o_t, W_t)
+        torch.cuda.synchronize()
+        ref = om.v_up(f64(o_t), f64(W_t))
+        assert_out_close(f64(out), ref, f"vup T={T} H={H}")
+
+
+def test_gather_bit_exact():
+    cfg = inputs.DecodeConfig(name="g", batch=5, heads=16, q_len=1, num_shards=2,
+                              block_size=16, ragged=(1, 150), seed=41)
+    prob = inputs.make_problem(cfg, seq_lens=[0, 1, 16, 17, 149])
+    dp = DeviceProblem(prob)
+    max_len = 160
+    dst = api.mla_gather_kv(dp.cache, dp.table, dp.lens, max_len, err_flag=dp.err)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    got = dst.view(torch.int16).cpu().numpy().view(np.uint16)
+    for b in range(cfg.batch):
+        L = int(prob.seq_lens[b])
+        want = om.gather_history(prob.kv_cache, prob.block_table[b], cfg.block_size, L)
+        assert np.array_equal(got[b, :L], want)
+        assert not got[b, L:].any()
+
+
+# ------------------------------------------------------------------ edge cases
+@pytest.mark.parametrize("lens", [[0, 0], [1, 31], [32, 64], [33, 97]])
+def test_edge_lengths(lens):
+    """Empty history (only the CURRENT part is visible), one token, exact
+    tile multiples and one-past-a-tile lengths."""
+    cfg = inputs.DecodeConfig(name="e", batch=2, heads=128, q_len=2, num_shards=3,
+                              block_size=32, ragged=(1, 100), current=True, seed=51)
+    dp = DeviceProblem(inputs.make_problem(cfg, seq_lens=lens))
+    o_part, lse_part = dp.partial()
+    out = api.mla_lse_combine_vup(o_part, lse_part, dp.W, err_flag=dp.err)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    _check_partials(dp, o_part, lse_part)
+    _, _, ref_out = om.decode_reference(dp.prob)
+    assert_out_close(f64(out), ref_out, "out")
+
+
+@pytest.mark.parametrize("gain", [30.0, 300.0])
+def test_peaked_logits_rescale(gain):
+    """q scaled up so the running max moves by many units across tiles: the
+    lazy O rescale must keep the result exact."""
+    cfg = inputs.DecodeConfig(name="pk", batch=2, heads=128, q_len=1, num_shards=2,
+                              block_size=32, history=700, q_gain=gain, seed=61)
+    dp = DeviceProblem(inputs.make_problem(cfg))
+    o_part, lse_part = dp.partial(part_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    _check_partials(dp, o_part, lse_part)
+
+
+def test_extreme_tile_late_in_shard():
+    """One tile late in a shard holds logits far above the rest (the slice
+    whose max dwarfs the others)."""
+    cfg = inputs.DecodeConfig(name="x", batch=1, heads=128, q_len=1, num_shards=2,
+                              block_size=32, history=512, shuffle_table=False, seed=71)
+    prob = inputs.make_problem(cfg)
+    # plant: q_abs[..., 0] = 4 for every head, and tokens 200..231 (tiles 6-7
+    # of shard 0, identity page table) carry c[0] large enough to lift their
+    # logits by about +30 over the rest
+    q = om.to_f64(prob.q_abs, "bf16")
+    q[0, 0, :, 0] = 4.0
+    prob.q_abs = inputs.round_to_bits(q.astype(np.float32), "bf16")
+    kv = om.to_f64(prob.kv_cache, "bf16")
+    flat = kv.reshape(-1, 576)
+    flat[200:232, 0] = 30.0 / (4.0 * cfg.scale)
+    prob.kv_cache = inputs.round_to_bits(kv.astype(np.float32), "bf16")
+    dp = DeviceProblem(prob)
+    o_part, lse_part = dp.partial(part_dtype=torch.float32)
+    torch.cuda.synchronize()
+    _check_partials(dp, o_part, lse_part)
+
+
+def test_equal_logit_rows():
+    cfg = inputs.DecodeConfig(name="eq", batch=3, heads=128, q_len=1, num_shards=4,
+                              block_size=32, ragged=(40, 500), dtype="fp16",
+                              part_dtype="fp16", equal_logit_rows=(1,), seed=81)
+    dp = DeviceProblem(inputs.make_problem(cfg))
+    out = dp.step()
+    torch.cuda.synchronize()
+    _, ref_l, ref_out = om.decode_reference(dp.prob)
+    assert_out_close(f64(out), ref_out, "out")
+
+
+# ------------------------------------------------------------------ streams and errors
+def test_user_stream_no_implicit_sync():
+    dp = DeviceProblem(inputs.make_problem(SMALL["ragged_bf16_cur"]))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = dp.step(stream=s)
+    s.synchronize()
+    _, _, ref_out = om.decode_reference(dp.prob)
+    assert_out_close(f64(out), ref_out, "out")
+
+
+def test_bad_block_id_sets_device_error():
+    cfg = inputs.DecodeConfig(name="bb", batch=2, heads=128, q_len=1, num_shards=2,
+                              block_size=32, history=100, seed=91)
+    prob = inputs.make_problem(cfg)
+    prob.block_table[1, 2] = prob.num_blocks + 5        # corrupt one entry
+    dp = DeviceProblem(prob)
+    dp.partial()
+    torch.cuda.synchronize()
+    assert dp.err.item() == 1
+    # the context is still usable
+    dp.err.zero_()
+    dp2 = DeviceProblem(inputs.make_problem(cfg))
+    dp2.partial()
+    torch.cuda.synchronize()
+    assert dp2.err.item() == 0
+
+
+def test_host_errors_launch_nothing():
+    dp = DeviceProblem(inputs.make_problem(inputs.CONFIGS["tiny"]))
+    with pytest.raises(api._ffi.MlaError) as e:
+        api.mla_dcp_decode_partial(dp.q_abs, dp.q_pe, dp.cache, dp.table, dp.lens, 65)
+    assert e.value.status == 5
+    with pytest.raises(api._ffi.MlaError) as e:
+        api.mla_dcp_decode_partial(dp.q_abs, dp.q_pe, dp.cache, dp.table, dp.lens, 2,
+                                   scale=-1.0)
+    assert e.value.status == 2
+
+
+# ------------------------------------------------------------------ full-size workloads
+@pytest.mark.parametrize("name", ["dsv3", "mtp", "ragged", "verylong"])
+def test_full_size_sampled(name):
+    """Full workload in the bench's launch configuration; checked on sampled
+    sequences and heads (every shard partial of those, and the final output)."""
+    cfg = inputs.CONFIGS[name]
+    prob = inputs.make_problem(cfg)
+    dp = DeviceProblem(prob)
+    o_part, lse_part = dp.partial()
+    out = api.mla_lse_combine_vup(o_part, lse_part, dp.W, err_flag=dp.err)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    rng = np.random.default_rng(7)
+    batch = sorted(set([0, cfg.batch - 1] + rng.integers(0, cfg.batch, 2).tolist()))
+    if cfg.equal_logit_rows:
+        batch = sorted(set(batch + [cfg.equal_logit_rows[0]]))
+    heads = sorted(set([0, cfg.heads - 1] + rng.integers(0, cfg.heads, 4).tolist()))
+    ref_po, ref_pl = om.decode_partials(prob, batch=batch, heads=heads)
+    got_po = f64(o_part[batch][:, :, :, heads])
+    got_pl = f64(lse_part[batch][:, :, :, heads])
+    assert_lse_close(got_pl, ref_pl, "lse_part")
+    assert_out_close(got_po, ref_po, "o_part")
+    ref_o, ref_l, ref_out = om.decode_reference(prob, batch=batch, heads=heads)
+    got = f64(out).reshape(cfg.batch, cfg.q_len, cfg.heads, 128)[batch][:, :, heads]
+    assert_out_close(got.reshape(ref_out.shape), ref_out, "out")

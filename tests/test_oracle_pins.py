@@ -85,6 +85,8 @@ def test_gather_tags_through_shuffled_table():
         assert list(got) == want
         fast = om.gather_history_fast(cache, p.block_table[b], 4, L)
         assert np.array_equal(fast, om.gather_history(cache, p.block_table[b], 4, L))
+    for gather in (om.gather_history, om.gather_history_fast):
+        assert gather(cache, p.block_table[0], 4, 0).shape == (0, 576)
     # every physical block is used by exactly one sequence
     used = p.block_table[p.block_table >= 0]
     assert sorted(used.tolist()) == list(range(p.num_blocks))
