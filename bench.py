@@ -1,0 +1,477 @@
+"""Benchmark of one decode step of MLA attention over a sharded latent KV cache.
+
+A step is the whole hot path on one batch: the per-shard partial attention
+kernel, then the fused LSE combine + V-up kernel.  The default workload is
+the DeepSeek-V3-shaped decode (batch 32, 128 heads, 4096 history tokens per
+sequence in 8 shards, 64-token pages with a shuffled block table, bf16).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is the KV-read rate in TB/s: the
+latent-KV bytes every step must read, divided by the device time per step.
+Inputs are larger than L2: each step uses the next of several layer caches
+(and W_UV copies), so no step finds the previous step's KV in L2.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload on this machine's host cores (the CPU baseline arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+# BLAS threads of the CPU oracle: every host core, stated in the output.
+_CPU_THREADS = os.cpu_count() or 1
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CPU_THREADS))
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mla_decode_attention_kv_gb300 import inputs  # noqa: E402
+
+METRIC = "MLA decode attn: KV-read TB/s, tokens/s, % of roofline at 1 GB300"
+L2_BYTES = 129 * 2 ** 20
+PROFILE = os.path.join(ROOT, "profiles", "partial_kernel_dsv3.md")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+WORKLOAD_TEXT = {
+    "dsv3": "DeepSeek-V3-shaped decode: batch 32, 128 heads, latent 512 + rope 64, 4096 KV "
+            "tokens each, 8 shards, paged cache block 64 with a shuffled block table, bf16 "
+            "N(0,1)*0.1, W_UV [128,512,128]",
+    "mtp": "long context MTP: batch 8, 128 heads, 32768 history tokens in 8 shards + current "
+           "chunk q_len 2 with a causal mask, bf16, block 32",
+    "ragged": "ragged mixed batch: batch 64, 128 heads, seq_lens log-uniform in [512,65536], "
+              "16 shards, block 32, random block table, fp16 cache",
+    "verylong": "very long context: batch 16, 128 heads, 131072 KV tokens, 16 shards, bf16, "
+                "fused combine + V-up",
+    "tiny": "tiny: batch 1, 16 heads, 256 history tokens in 2 shards + 1 current token",
+}
+
+
+# ------------------------------------------------------------------ work model
+def work_model(prob: inputs.DecodeProblem) -> dict:
+    """Algorithmic bytes / flops of one step (each byte the method must move
+    once; KV read once for all heads)."""
+    cfg = prob.cfg
+    B, q, H, P = cfg.batch, cfg.q_len, cfg.heads, prob.num_parts
+    T = B * q
+    esz = 2
+    psz = 4 if cfg.part_dtype == "fp32" else 2
+    kv = inputs.kv_bytes(prob)
+    q_bytes = T * H * inputs.D_QK * esz
+    opart = T * P * H * inputs.D_LATENT * psz
+    lsep = T * P * H * 4
+    w = H * inputs.D_LATENT * inputs.D_V * esz
+    out = T * H * inputs.D_V * esz
+    hist = prob.seq_lens.astype(np.int64)
+    cur = q if prob.kv_cur is not None else 0
+    # visible (query, key) pairs; each costs 2*H*(576 + 512) flops
+    pairs = int(hist.sum()) * q + B * (q * (q + 1) // 2 if cur else 0)
+    attn_flops = 2 * H * (inputs.D_QK + inputs.D_LATENT) * pairs
+    vup_flops = 2 * T * H * inputs.D_LATENT * inputs.D_V
+    return {
+        "kv_bytes": kv,
+        "partial_bytes": kv + q_bytes + opart + lsep,
+        "partial_flops": attn_flops,
+        "combine_vup_bytes": opart + lsep + w + out,
+        "step_bytes": kv + q_bytes + 2 * (opart + lsep) + w + out,
+        "step_flops": attn_flops + vup_flops,
+        "query_tokens": T,
+        "h2d_bytes": q_bytes + prob.block_table.nbytes + prob.seq_lens.nbytes
+        + (prob.kv_cur.nbytes if prob.kv_cur is not None else 0),
+        "d2h_bytes": out,
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, \
+            "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_decode_attention_kv_gb300", "csrc")
+    for name in ("partial.cu", "ptx.cuh", "common.cuh", "kernels.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(config_name: str):
+    """DRAM bytes per launch of the partial kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    key = f"dram_bytes_per_launch_{config_name}"
+    try:
+        return float(fields[key])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append({"t": ts + frac, "sm": float(parts[2]), "max": float(parts[3]),
+                             "power": float(parts[4]) if parts[4] not in ("[N/A]", "") else None,
+                             "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
+                             "sw_power": parts[9]})
+            except (ValueError, IndexError):
+                continue
+        os.unlink(self.path)
+        return rows
+
+    @staticmethod
+    def summarize(rows, t0, t1):
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.06 <= r["t"] <= t1 + 0.06]
+        used = inside or sorted(rows, key=lambda r: abs(r["t"] - (t0 + t1) / 2))[:3]
+        reasons = set()
+        for r in used:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in used),
+                "sm_max_mhz": max(r["max"] for r in used),
+                "reasons": sorted(reasons), "samples": len(used),
+                "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from mla_decode_attention_kv_gb300 import api, build as mbuild
+    from mla_decode_attention_kv_gb300 import _ffi
+
+    mbuild.build()
+    _ffi.lib()
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    cfg = inputs.CONFIGS[args.config]
+    prob = inputs.make_problem(cfg)
+    wm = work_model(prob)
+    dt = api.torch_dtype(cfg.dtype)
+    pdt = api.torch_dtype(cfg.part_dtype)
+
+    def t16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt)
+
+    q_abs, q_pe, W0 = t16(prob.q_abs), t16(prob.q_pe), t16(prob.W_UV)
+    cache0 = t16(prob.kv_cache)
+    kv_cur = t16(prob.kv_cur) if prob.kv_cur is not None else None
+    table = torch.from_numpy(prob.block_table).to(dev)
+    lens = torch.from_numpy(prob.seq_lens).to(dev)
+    per_layer = cache0.numel() * 2 + W0.numel() * 2
+    layers = args.layers or max(2, math.ceil(4 * L2_BYTES / per_layer))
+    caches = [cache0] + [cache0.clone() for _ in range(layers - 1)]
+    Ws = [W0] + [W0.clone() for _ in range(layers - 1)]
+    B, q, H, P = cfg.batch, cfg.q_len, cfg.heads, prob.num_parts
+    o_part = torch.empty((B, q, P, H, 512), dtype=pdt, device=dev)
+    lse_part = torch.empty((B, q, P, H), dtype=torch.float32, device=dev)
+    out = torch.empty((B * q, H * 128), dtype=dt, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        li = i % layers
+        if ev is not None:
+            ev[0].record(stream)
+        api.mla_dcp_decode_partial(q_abs, q_pe, caches[li], table, lens, cfg.num_shards,
+                                   kv_cur=kv_cur, scale=cfg.scale, o_part=o_part,
+                                   lse_part=lse_part, err_flag=err, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        api.mla_lse_combine_vup(o_part, lse_part, Ws[li], out=out, err_flag=err, stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    w0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, kev[i])
+    e1.record(stream)
+    barrier()
+    w1 = time.time()
+    total_ms = e0.elapsed_time(e1)
+    partial_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
+    if err.item() != 0:
+        raise RuntimeError(f"device error {err.item()} during the timed region")
+
+    # ---- end to end through the public API with pinned host buffers
+    def pin(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+    h_qa = pin(prob.q_abs.view(np.int16))
+    h_qp = pin(prob.q_pe.view(np.int16))
+    h_tab = pin(prob.block_table)
+    h_len = pin(prob.seq_lens)
+    h_cur = pin(prob.kv_cur.view(np.int16)) if prob.kv_cur is not None else None
+    h_out = torch.empty((B * q, H * 128), dtype=torch.int16).pin_memory()
+    d_qa = torch.empty_like(q_abs)
+    d_qp = torch.empty_like(q_pe)
+    d_tab = torch.empty_like(table)
+    d_len = torch.empty_like(lens)
+    d_cur = torch.empty_like(kv_cur) if kv_cur is not None else None
+
+    def e2e_step(i):
+        li = i % layers
+        d_qa.view(torch.int16).copy_(h_qa, non_blocking=True)
+        d_qp.view(torch.int16).copy_(h_qp, non_blocking=True)
+        d_tab.copy_(h_tab, non_blocking=True)
+        d_len.copy_(h_len, non_blocking=True)
+        if d_cur is not None:
+            d_cur.view(torch.int16).copy_(h_cur, non_blocking=True)
+        api.decode_step(d_qa, d_qp, caches[li], d_tab, d_len, Ws[li], cfg.num_shards,
+                        kv_cur=d_cur, scale=cfg.scale, o_part=o_part, lse_part=lse_part,
+                        out=out, err_flag=err, stream=stream)
+        h_out.copy_(out.view(torch.int16), non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for i in range(args.steps):
+        e2e_step(args.warmup + i)
+    f1.record(stream)
+    barrier()
+    e2e_ms = f0.elapsed_time(f1)
+    clocks = ClockSampler.summarize(sampler.stop(), w0, w1) if sampler else None
+
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_ms, partial_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms, partial_ms = t.tolist()
+    if rank != 0:
+        return None
+
+    ms_per_step = total_ms / args.steps
+    kv_tbs = world * wm["kv_bytes"] / (ms_per_step * 1e-3) / 1e12
+    tok_s = world * wm["query_tokens"] / (ms_per_step * 1e-3)
+    e2e_tbs = world * wm["kv_bytes"] / (e2e_ms / args.steps * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    part_s = partial_ms * 1e-3
+    hbm_ach = wm["partial_bytes"] / part_s / 1e9
+    tc_ach = wm["partial_flops"] / part_s / 1e12
+    hbm_frac = hbm_ach / peaks["hbm_gbs"]
+    tc_frac = tc_ach / peaks["bf16_tflops"]
+    if hbm_frac >= tc_frac:
+        roof = {"bound": "hbm", "achieved": round(hbm_ach, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(hbm_frac, 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(tc_ach, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(tc_frac, 4)}
+    roof["traffic"] = traffic_from_profile(args.config)
+    roof["kernel"] = "mla_partial_kernel"
+    roof["kernel_ms"] = round(partial_ms, 5)
+    roof["alg_bytes_per_launch"] = wm["partial_bytes"]
+    roof["alg_flops_per_launch"] = wm["partial_flops"]
+    roof["tensor_frac"] = round(tc_frac, 4)
+    roof["hbm_frac"] = round(hbm_frac, 4)
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" \
+        else "fallback"
+    step_s = ms_per_step * 1e-3
+    step_roof = max(wm["step_bytes"] / (peaks["hbm_gbs"] * 1e9),
+                    wm["step_flops"] / (peaks["bf16_tflops"] * 1e12)) / step_s
+    line = {
+        "metric": METRIC,
+        "value": round(kv_tbs, 4),
+        "unit": "TB/s",
+        "tokens_per_s": round(tok_s, 1),
+        "step_roofline_frac": round(step_roof, 4),
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config,
+                   "query_tokens_per_step": wm["query_tokens"],
+                   "kv_bytes_per_step": wm["kv_bytes"],
+                   "l2": f"inputs larger than L2: {layers} rotated layer caches + W_UV "
+                         f"({layers * per_layer / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "e2e": {"value": round(e2e_tbs, 4), "unit": "TB/s",
+                "h2d_bytes_per_step": wm["h2d_bytes"], "d2h_bytes_per_step": wm["d2h_bytes"]},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(prob, args.cpu_seconds)
+    return line
+
+
+# ------------------------------------------------------------------ CPU oracle
+def _oracle_sample(prob, batch):
+    from oracle import mla_oracle as om
+    om.decode_reference(prob, batch=batch)
+
+
+def cpu_baseline(prob, budget_s: float):
+    """The oracle as it stands on the host cores, on a bounded sample of the
+    workload (whole sequences, all heads), scaled to KV-read TB/s."""
+    cfg = prob.cfg
+    t0 = time.perf_counter()
+    _oracle_sample(prob, [0])
+    one = time.perf_counter() - t0
+    n = int(max(1, min(cfg.batch, budget_s / max(one, 1e-3))))
+    batch = list(range(n))
+    t0 = time.perf_counter()
+    _oracle_sample(prob, batch)
+    dt = time.perf_counter() - t0
+    kv = int(prob.seq_lens[:n].astype(np.int64).sum()) * inputs.D_QK * 2
+    return {"value": round(kv / dt / 1e12, 9), "unit": "TB/s", "cores": _CPU_THREADS,
+            "kind": "oracle",
+            "sample": f"{n} of {cfg.batch} sequences (all {cfg.heads} heads, full history) "
+                      f"in {dt:.1f} s, fp64 numpy oracle, {_CPU_THREADS} BLAS threads"}
+
+
+def run_reference(args, rank, world):
+    """CPU baseline arm: the oracle timed as it stands on the host cores."""
+    if rank != 0:
+        return None
+    cfg = inputs.CONFIGS[args.config]
+    prob = inputs.make_problem(cfg)
+    per_seq = int(prob.seq_lens[0]) * inputs.D_QK * 2
+    for i in range(args.warmup):
+        _oracle_sample(prob, [i % cfg.batch])
+    times = []
+    kv = 0
+    for i in range(args.steps):
+        b = (args.warmup + i) % cfg.batch
+        t0 = time.perf_counter()
+        _oracle_sample(prob, [b])
+        times.append(time.perf_counter() - t0)
+        kv += int(prob.seq_lens[b]) * inputs.D_QK * 2
+    total = sum(times)
+    value = kv / total / 1e12
+    sample = (f"each step: 1 of {cfg.batch} sequences (all {cfg.heads} heads, "
+              f"{int(prob.seq_lens[0])} history tokens, {per_seq / 1e6:.1f} MB KV)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 9), "unit": "TB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 9), "unit": "TB/s", "cores": _CPU_THREADS,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 9), "unit": "TB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(inputs.CONFIGS), default="dsv3")
+    ap.add_argument("--layers", type=int, default=0, help="layer caches rotated (0 = auto)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="budget of the CPU-oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+        line = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
