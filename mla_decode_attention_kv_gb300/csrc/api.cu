@@ -107,11 +107,10 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
     return MLA_ERR_MISALIGNED;
 
   const bool bf16 = in_dtype == MLA_BF16;
-  const int box_rows = block_size < mla::kPartialTile ? block_size : mla::kPartialTile;
+  const int box_rows = block_size < mla::kPartialBox ? block_size : mla::kPartialBox;
   const uint64_t qrows = static_cast<uint64_t>(B) * q_len * H;
-  CUtensorMap tm_qabs, tm_qpe, tm_kv, tm_cur;
-  if (!make_map(&tm_qabs, q_abs, 512, qrows, 1024, 64, 128, bf16) ||
-      !make_map(&tm_qpe, q_pe, 64, qrows, 128, 64, 128, bf16) ||
+  CUtensorMap tm_qpe, tm_kv, tm_cur;
+  if (!make_map(&tm_qpe, q_pe, 64, qrows, 128, 64, 128, bf16) ||
       !make_map(&tm_kv, kv_cache, 576, static_cast<uint64_t>(num_blocks) * block_size, 1152, 64,
                 box_rows, bf16))
     return MLA_ERR_CUDA;
@@ -144,7 +143,7 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
   pp.box_rows = box_rows;
   pp.scale_log2 = scale * 1.4426950408889634f;
   pp.part_dtype = part_dtype;
-  return launched(mla::launch_partial(tm_qabs, tm_qpe, tm_kv, tm_cur, pp, bf16,
+  return launched(mla::launch_partial(tm_qpe, tm_kv, tm_cur, q_abs, pp, bf16,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -15,17 +15,16 @@ struct PartialParams {
   int* err;
   int B, q_len, H, num_blocks, bs, max_blocks, S, P, has_cur;
   int num_units;
-  int box_rows;          // rows per TMA box of the KV maps: min(tile, block_size)
+  int box_rows;          // rows per TMA box of the KV maps: min(32, block_size)
   float scale_log2;      // softmax scale * log2(e)
   int part_dtype;        // 0 bf16, 1 fp16, 2 fp32
 };
 
-// Tokens per KV tile of the partial kernel.
-constexpr int kPartialTile = 32;
+// Rows per TMA box of the partial kernel's KV maps: min(kPartialBox, bs).
+constexpr int kPartialBox = 32;
 
-int launch_partial(const CUtensorMap& qabs, const CUtensorMap& qpe, const CUtensorMap& kv,
-                   const CUtensorMap& cur, const PartialParams& pp, bool bf16,
-                   cudaStream_t stream);
+int launch_partial(const CUtensorMap& qpe, const CUtensorMap& kv, const CUtensorMap& cur,
+                   const void* q_abs, const PartialParams& pp, bool bf16, cudaStream_t stream);
 int launch_combine(const void* o_part, const float* lse_part, int P, const void* o_local,
                    const float* lse_local, int T, int H, int part_dt, int out_dt, void* o_latent,
                    float* lse_out, cudaStream_t stream);

@@ -8,29 +8,33 @@
 // HISTORY and CURRENT attention calls of code blocks B and C).
 //
 // Work unit = (sequence b, query token i, part p).  Per unit, with the 128
-// query heads of token i as the M dimension:
-//   S = Q . K^T        Q [128 x 576], K = tile of TILE cached tokens x 576
-//   P = exp2(S*scale*log2e - m)    (online softmax, running max m, lazy rescale)
-//   O += P . V         V = the same tile's latent columns, [TILE x 512]
+// query heads of token i as the M dimension of every MMA:
+//   S = Q . K^T        Q [128 x 576], K = tile of 128 cached tokens x 576
+//   P = exp2(S*scale*log2e - m)   online softmax (running max m, lazy rescale)
+//   O += P . V         V = the same tokens' latent columns, [128 x 512]
 //
-// GB300 mapping.  A 128 x 512 fp32 accumulator alone fills an SM's whole
-// tensor memory (128 lanes x 512 columns), so each unit runs on a CLUSTER OF
-// TWO CTAs on two SMs:
-//   CTA 0 owns latent chunks 0..3 (dims 0..255) and the RoPE chunk (512..575)
-//   CTA 1 owns latent chunks 4..7 (dims 256..511)
-// Each CTA TMA-loads only its own 64-dim chunks of Q and of every KV tile, so
-// each KV byte crosses HBM exactly once.  Each CTA computes the partial
-// S_r = Q_r . K_r^T over its chunks on its tensor cores; the two fp32
-// partials are swapped through distributed shared memory and summed, so both
-// CTAs hold the same S, take the same softmax and produce the same P.  Each
-// CTA then accumulates its 256-column half of O = P . V_r in TMEM.
+// GB300 mapping: a SPLIT-ROLE PAIR of CTAs (a 2-CTA cluster on two SMs).
+// A 128 x 512 fp32 accumulator fills one SM's whole tensor memory, and
+// tensor-core MMAs only run at full rate with N >= 128, so the work is split
+// by role rather than by data:
+//   rank 0 ("QK CTA"): Q's latent part lives in its TMEM (the A operand of
+//     tcgen05 MMAs straight from tensor memory), the RoPE part in SMEM;
+//     S = Q K^T for 128-token tiles (N = 128) into two TMEM buffers; online
+//     softmax; P (bf16/fp16) plus per-row rescale factors and final row sums
+//     are shipped to rank 1 with one shared-memory-to-shared-memory bulk copy
+//     per tile (DSMEM, 256 B per token, one direction).
+//   rank 1 ("PV CTA"): the full fp32 O [128 x 512] in its TMEM; O += P V with
+//     N = 256 MMAs; rescale of O when the running max moved; epilogue O / l.
+// Each CTA TMA-loads the KV columns it needs (rank 0 all 576, rank 1 the 512
+// latent ones, close in time so the second read hits L2).
 //
-// Roles per CTA (256 threads):
-//   warp 0       TMA producer: Q once per unit, KV tiles into a STAGES ring
-//   warp 1       MMA issuer (tcgen05, one elected thread); owns TMEM
-//   warps 4..7   softmax + S exchange + O rescale + epilogue (thread = head)
+// Warp roles (256 threads per CTA):
+//   rank 0: w0 TMA producer (K chunks + Q RoPE), w1 MMA issuer, w2-3 LSE of
+//           empty parts, w4-7 softmax + Q latent loader (thread = head row)
+//   rank 1: w0 TMA producer (V), w1 MMA issuer, w2 hands P buffers back,
+//           w3 zeros of empty parts, w4-7 O rescale + epilogue (thread = row)
 // Every wait is bounded; on timeout the kernel records MLA_DEV_WAIT_TIMEOUT,
-// drains its own copies and MMAs, frees TMEM and returns.
+// raises an abort flag, drains its own copies and MMAs, frees TMEM, returns.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -39,9 +43,11 @@ namespace mla {
 // Token range of one unit.  History shard p of sequence b covers
 // [p*len, min(L, (p+1)*len)), len = bs * ceil(L / (S*bs)) (block-aligned,
 // trailing shards possibly empty).  The CURRENT part covers kv_cur[b, 0..i].
+// Units are numbered u = ((b * q_len + i) * P + p), so the parts of one query
+// token are consecutive and a cluster walking a contiguous range reuses Q.
 struct UnitInfo {
   int b, i, p;
-  int lo, hi;      // token range inside the part's token space
+  int lo, hi;
   bool current;
   int ntiles;
 };
@@ -49,10 +55,10 @@ struct UnitInfo {
 template <int TILE>
 __device__ __forceinline__ UnitInfo unit_info(const PartialParams& pp, int u) {
   UnitInfo ui;
-  ui.i = u % pp.q_len;
-  int bp = u / pp.q_len;
-  ui.p = bp % pp.P;
-  ui.b = bp / pp.P;
+  ui.p = u % pp.P;
+  const int bi = u / pp.P;
+  ui.i = bi % pp.q_len;
+  ui.b = bi / pp.q_len;
   ui.current = pp.has_cur && ui.p == pp.S;
   if (ui.current) {
     ui.lo = 0;
@@ -60,8 +66,8 @@ __device__ __forceinline__ UnitInfo unit_info(const PartialParams& pp, int u) {
   } else {
     int L = pp.seq_lens[ui.b];
     L = max(0, min(L, pp.max_blocks * pp.bs));
-    int chunk = pp.S * pp.bs;
-    int len = L > 0 ? pp.bs * ((L + chunk - 1) / chunk) : 0;
+    const int chunk = pp.S * pp.bs;
+    const int len = L > 0 ? pp.bs * ((L + chunk - 1) / chunk) : 0;
     ui.lo = min(L, ui.p * len);
     ui.hi = min(L, (ui.p + 1) * len);
   }
@@ -69,83 +75,150 @@ __device__ __forceinline__ UnitInfo unit_info(const PartialParams& pp, int u) {
   return ui;
 }
 
-template <int TILE, int STAGES>
-struct PartialSmem {
-  static constexpr int kChunks = 5;                       // CTA 0: 4 latent + RoPE
-  static constexpr int kQBytes = kChunks * 128 * 128;     // 80 KB
-  static constexpr int kChunkBytes = TILE * 128;          // one 64-dim chunk of a tile
-  static constexpr int kStageBytes = kChunks * kChunkBytes;
-  static constexpr int kPBytes = TILE == 32 ? 16384 : 32768;   // two P buffers
-  static constexpr int kXBytes = 128 * TILE * 4;          // one exchange buffer
-  static constexpr int kQOff = 0;
-  static constexpr int kKVOff = kQOff + kQBytes;
-  static constexpr int kPOff = kKVOff + STAGES * kStageBytes;
-  static constexpr int kXOff = kPOff + kPBytes;
-  static constexpr int kBarOff = kXOff + 2 * kXBytes;
-  static constexpr int kTotal = kBarOff + 256 + 1024;     // barriers + 1 KB align slack
+// Walks the tiles of the non-empty units in [u0, u1) as one flat stream.
+template <int TILE>
+struct TileIter {
+  int u, u_end, j, k, nq, qkey;
+  bool newq, valid;
+  UnitInfo ui;
+  __device__ __forceinline__ void start(const PartialParams& pp, int u0, int u1) {
+    u = u0 - 1;
+    u_end = u1;
+    k = -1;
+    nq = -1;
+    qkey = -1;
+    valid = true;
+    next_unit(pp);
+  }
+  __device__ __forceinline__ void next_unit(const PartialParams& pp) {
+    for (++u; u < u_end; ++u) {
+      ui = unit_info<TILE>(pp, u);
+      if (ui.ntiles > 0) {
+        ++k;
+        j = 0;
+        const int key = ui.b * pp.q_len + ui.i;
+        newq = key != qkey;
+        if (newq) {
+          ++nq;
+          qkey = key;
+        }
+        return;
+      }
+    }
+    valid = false;
+  }
+  __device__ __forceinline__ void advance(const PartialParams& pp) {
+    if (++j >= ui.ntiles) next_unit(pp);
+  }
+  __device__ __forceinline__ bool first() const { return j == 0; }
+  __device__ __forceinline__ bool last() const { return j == ui.ntiles - 1; }
+  // Whether this tile is the last one that reads the current Q.
+  __device__ __forceinline__ bool last_of_q(const PartialParams& pp) const {
+    if (!last()) return false;
+    TileIter n = *this;
+    n.next_unit(pp);
+    return !n.valid || n.newq;
+  }
 };
 
-template <int TILE, int STAGES, bool BF16>
+// Shared-memory plan (offsets from a 1024-aligned base; same size on both
+// ranks).  Rank 0: K chunk ring, Q RoPE tile, two outgoing P messages.
+// Rank 1: V ring, two incoming P messages.  Barriers at one common offset.
+struct PairSmem {
+  static constexpr int kTile = 128;
+  static constexpr int kKStage = kTile * 128;          // one 64-dim chunk of a tile
+  static constexpr int kNK = 8;
+  static constexpr int kVSub = 32;                     // tokens per V stage
+  static constexpr int kVChunk = kVSub * 128;          // one 64-dim chunk of a V stage
+  static constexpr int kVStage = 8 * kVChunk;          // 32 tokens x 512 latent
+  static constexpr int kNV = 4;
+  // P message: P [128 rows x 128 tokens] as two 64-token SW128 chunks,
+  // alpha[128], lsum[128], header.
+  static constexpr int kMsgP = 2 * 16384;
+  static constexpr int kMsgAlpha = kMsgP;
+  static constexpr int kMsgL = kMsgAlpha + 512;
+  static constexpr int kMsgHdr = kMsgL + 512;
+  static constexpr int kMsgBytes = kMsgHdr + 16;       // 33808, multiple of 16
+  static constexpr int kMsgStride = 34816;             // 1024-aligned slot
+  // rank 0
+  static constexpr int kKOff = 0;
+  static constexpr int kQrOff = kKOff + kNK * kKStage;       // 131072
+  static constexpr int kPsOff = kQrOff + 16384;              // 147456
+  // rank 1
+  static constexpr int kVOff = 0;
+  static constexpr int kPrOff = kVOff + kNV * kVStage;       // 131072
+  static constexpr int kBarOff = kPsOff + 2 * kMsgStride;    // 217088
+  static constexpr int kTotal = kBarOff + 512 + 1024;
+};
+static_assert(PairSmem::kPrOff + 2 * PairSmem::kMsgStride <= PairSmem::kBarOff, "rank-1 plan");
+static_assert(PairSmem::kTotal <= 232448, "shared memory budget");
+
+// Barrier slots in the common block.
+enum : int {
+  B_KFULL = 0, B_KEMPTY = 8, B_QR_FULL = 16, B_Q_EMPTY = 17, B_QLAT_FULL = 18, B_S_FULL = 19,
+  B_S_EMPTY = 21, B_PFREE = 23, B_MMA_DONE_A = 25,
+  B_VFULL = 26, B_VEMPTY = 30, B_P_FULL = 34, B_PV_DONE = 36, B_META_READ = 38, B_O_EMPTY = 40,
+  B_O_FIXED = 41, B_MMA_DONE_B = 42, B_COUNT = 43
+};
+
+template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
-    mla_partial_kernel(const __grid_constant__ CUtensorMap tm_qabs,
-                       const __grid_constant__ CUtensorMap tm_qpe,
+    mla_partial_kernel(const __grid_constant__ CUtensorMap tm_qpe,
                        const __grid_constant__ CUtensorMap tm_kv,
-                       const __grid_constant__ CUtensorMap tm_cur, const PartialParams pp) {
-  using L = PartialSmem<TILE, STAGES>;
-  static_assert(TILE == 32 || TILE == 64, "TILE");
-  static_assert(L::kTotal <= 232448, "shared memory budget");
+                       const __grid_constant__ CUtensorMap tm_cur, const uint16_t* __restrict__ q_abs,
+                       const PartialParams pp) {
+  using L = PairSmem;
+  constexpr int TILE = L::kTile;
   constexpr int kTmemCols = 512;
-  constexpr uint32_t kOCol = 0;          // O half: columns [0, 256)
-  constexpr uint32_t kSCol = 256;        // S buffers: [256, 256 + 2*TILE)
+  constexpr uint32_t kQlatCol = 0;       // rank 0: Q latent, 256 packed columns
+  constexpr uint32_t kSCol = 256;        // rank 0: S buffers [256,384), [384,512)
   constexpr float kRescaleThresh = 8.0f; // lazy rescale: only when max grows by > 2^8
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem + L::kQOff;
-  uint8_t* sKV = smem + L::kKVOff;
-  uint8_t* sP = smem + L::kPOff;
-  uint8_t* sX = smem + L::kXOff;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* kv_full = bars;                 // [STAGES]
-  uint64_t* kv_empty = bars + STAGES;       // [STAGES]
-  uint64_t* q_full = bars + 2 * STAGES;
-  uint64_t* q_empty = q_full + 1;
-  uint64_t* s_full = q_full + 2;            // [2]
-  uint64_t* s_empty = q_full + 4;           // [2]
-  uint64_t* p_full = q_full + 6;            // [2]
-  uint64_t* p_empty = q_full + 8;           // [2]
-  uint64_t* x_full = q_full + 10;           // [2]  arrived by the peer
-  uint64_t* x_empty = q_full + 12;          // [2]  arrived by the peer
-  uint64_t* o_empty = q_full + 14;
-  uint64_t* mma_done = q_full + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(q_full + 17);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + B_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + B_COUNT + 1);
+  volatile uint32_t* warp_flags = reinterpret_cast<volatile uint32_t*>(bar + B_COUNT + 2);
 
   const uint32_t rank = cluster_ctarank();
-  const uint32_t peer = rank ^ 1u;
-  const int nch = rank == 0 ? 5 : 4;        // chunks owned by this CTA
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int* err = pp.err;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    if (rank == 0) {
+      for (int s = 0; s < L::kNK; ++s) {
+        mbar_init(&bar[B_KFULL + s], 1);
+        mbar_init(&bar[B_KEMPTY + s], 1);
+      }
+      mbar_init(&bar[B_QR_FULL], 1);
+      mbar_init(&bar[B_Q_EMPTY], 1);
+      mbar_init(&bar[B_QLAT_FULL], 4);
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(&bar[B_S_FULL + k], 1);
+        mbar_init(&bar[B_S_EMPTY + k], 4);
+        mbar_init(&bar[B_PFREE + k], 1);
+      }
+      mbar_init(&bar[B_MMA_DONE_A], 1);
+    } else {
+      for (int s = 0; s < L::kNV; ++s) {
+        mbar_init(&bar[B_VFULL + s], 1);
+        mbar_init(&bar[B_VEMPTY + s], 1);
+      }
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(&bar[B_P_FULL + k], 1);
+        mbar_init(&bar[B_PV_DONE + k], 1);
+        mbar_init(&bar[B_META_READ + k], 4);
+      }
+      mbar_init(&bar[B_O_EMPTY], 4);
+      mbar_init(&bar[B_O_FIXED], 4);
+      mbar_init(&bar[B_MMA_DONE_B], 1);
+      // the first two P messages may land as soon as the cluster is up
+      mbar_arrive_expect_tx(&bar[B_P_FULL + 0], L::kMsgBytes);
+      mbar_arrive_expect_tx(&bar[B_P_FULL + 1], L::kMsgBytes);
     }
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(&s_full[k], 1);
-      mbar_init(&s_empty[k], 4);
-      mbar_init(&p_full[k], 4);
-      mbar_init(&p_empty[k], 1);
-      mbar_init(&x_full[k], 4);
-      mbar_init(&x_empty[k], 4);
-    }
-    mbar_init(o_empty, 4);
-    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -154,203 +227,221 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tm_qabs);
     prefetch_tmap(&tm_qpe);
     prefetch_tmap(&tm_kv);
     prefetch_tmap(&tm_cur);
   }
   __syncthreads();
-  cluster_sync();  // peer barriers are initialised before any remote arrive
+  cluster_sync();   // every barrier of both CTAs is initialised
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // contiguous range of units of this cluster
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(nclusters_x());
+  const int u0 = static_cast<int>(static_cast<int64_t>(cid) * pp.num_units / ncl);
+  const int u1 = static_cast<int>(static_cast<int64_t>(cid + 1) * pp.num_units / ncl);
 
-  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+  auto wait = [&](uint64_t* b, uint32_t parity) -> bool {
     for (uint32_t it = 0; it < kSpinLimit; ++it) {
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait(b, parity)) return true;
       if ((it & 1023u) == 1023u && *abort_flag) return false;
     }
     set_error(err, kDevWaitTimeout);
     *abort_flag = 1;
     return false;
   };
-  auto wait_cl = [&](uint64_t* bar, uint32_t parity) -> bool {
+  auto wait_cl = [&](uint64_t* b, uint32_t parity) -> bool {
     for (uint32_t it = 0; it < kSpinLimit; ++it) {
-      if (mbar_try_wait_cluster(bar, parity)) return true;
+      if (mbar_try_wait_cluster(b, parity)) return true;
       if ((it & 1023u) == 1023u && *abort_flag) return false;
     }
     set_error(err, kDevWaitTimeout);
     *abort_flag = 1;
     return false;
   };
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol_stream = policy_evict_first();   // KV is read once
-      const uint64_t pol_keep = policy_evict_last();      // Q is shared by units
-      int g = 0, k = 0;
-      int last_g[STAGES];
-      for (int s = 0; s < STAGES; ++s) last_g[s] = -1;
-      int q_issued = 0;
-      bool ok = true;
-      for (int u = cid; u < pp.num_units && ok; u += ncl) {
-        UnitInfo ui = unit_info<TILE>(pp, u);
-        if (ui.ntiles == 0) continue;
-        if (k >= 1 && !wait(q_empty, (k - 1) & 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(q_full, nch * 16384);
-        const int qrow = (ui.b * pp.q_len + ui.i) * pp.H;
-        for (int c = 0; c < nch; ++c) {
-          if (rank == 0 && c == 4)
-            tma_load_2d(sQ + c * 16384, &tm_qpe, q_full, 0, qrow, pol_keep);
-          else
-            tma_load_2d(sQ + c * 16384, &tm_qabs, q_full, (rank * 4 + c) * 64, qrow, pol_keep);
-        }
-        q_issued = k + 1;
-        for (int j = 0; j < ui.ntiles; ++j, ++g) {
-          const int st = g % STAGES;
-          if (g >= STAGES && !wait(&kv_empty[st], ((g / STAGES) - 1) & 1)) { ok = false; break; }
-          uint8_t* dst = sKV + st * L::kStageBytes;
-          mbar_arrive_expect_tx(&kv_full[st], nch * L::kChunkBytes);
-          const int t0 = ui.lo + j * TILE;
-          for (int sub = 0; sub < TILE / pp.box_rows; ++sub) {
-            int row;
-            const CUtensorMap* map;
-            if (ui.current) {
-              row = ui.b * pp.q_len + sub * pp.box_rows;
-              map = &tm_cur;
-            } else {
-              int t = t0 + sub * pp.box_rows;
-              // sub-boxes past the unit's last token re-read its last page
-              // (in bounds, finite, masked out by the softmax)
-              if (t >= ui.hi) t = ui.hi - 1;
-              const int lb = t / pp.bs;
-              int pb = pp.block_table[static_cast<int64_t>(ui.b) * pp.max_blocks + lb];
-              if (pb < 0 || pb >= pp.num_blocks) {
-                set_error(err, kDevBadBlockId);
-                pb = 0;
-              }
-              row = pb * pp.bs + (t % pp.bs);
-              if (t != t0 + sub * pp.box_rows) row -= row % pp.box_rows;
-              map = &tm_kv;
-            }
-            for (int c = 0; c < nch; ++c) {
-              const int x = (rank == 0 && c == 4) ? 512 : (rank * 4 + c) * 64;
-              tma_load_2d(dst + c * L::kChunkBytes + sub * pp.box_rows * 128, map, &kv_full[st], x,
-                          row, pol_stream);
-            }
-          }
-          last_g[st] = g;
-        }
-        ++k;
-      }
-      // drain: every issued copy has landed before this CTA may exit
-      for (int s = 0; s < STAGES; ++s)
-        if (last_g[s] >= 0) mbar_wait(&kv_full[s], (last_g[s] / STAGES) & 1, err);
-      if (q_issued > 0) mbar_wait(q_full, (q_issued - 1) & 1, err);
+  // Row (in the KV map) of TMA box `l` of the tile starting at token t0 of
+  // the unit; boxes past the unit's end re-read its last box (in bounds,
+  // masked out by the softmax).
+  auto box_row = [&](const UnitInfo& ui, int t0, int l) -> int {
+    if (ui.current) return ui.b * pp.q_len + l * pp.box_rows;
+    int t = t0 + l * pp.box_rows;
+    const bool past = t >= ui.hi;
+    if (past) t = ui.hi - 1;
+    int pb = pp.block_table[static_cast<int64_t>(ui.b) * pp.max_blocks + t / pp.bs];
+    if (pb < 0 || pb >= pp.num_blocks) {
+      set_error(err, kDevBadBlockId);
+      pb = 0;
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = make_idesc_f16(128, TILE, BF16, false, false);
-      constexpr uint32_t idesc_pv = make_idesc_f16(128, 256, BF16, false, true);
-      const uint32_t q_base = smem_u32(sQ);
-      const uint32_t kv_base = smem_u32(sKV);
-      const uint32_t p_base = smem_u32(sP);
-      int g = 0, k = 0;
+    int row = pb * pp.bs + (t % pp.bs);
+    if (past) row -= row % pp.box_rows;
+    return row;
+  };
+  const int nbox = TILE / pp.box_rows;    // TMA boxes per tile and chunk (4 or 8)
+
+  if (rank == 0) {
+    uint8_t* sK = smem + L::kKOff;
+    uint8_t* sQr = smem + L::kQrOff;
+    uint8_t* sPs = smem + L::kPsOff;
+    if (warp == 0) {
+      // ------------------------------------------------ rank 0: TMA producer
+      const uint64_t pol_kv = policy_evict_last();     // rank 1 re-reads the latent
+      const uint64_t pol_q = policy_evict_last();
+      TileIter<TILE> it;
+      it.start(pp, u0, u1);
+      int cs = 0;
+      int last_cs[L::kNK];
+#pragma unroll
+      for (int s = 0; s < L::kNK; ++s) last_cs[s] = -1;
+      int qloads = 0;
       bool ok = true;
-      auto issue_pv = [&](int gg, bool first) -> bool {
-        const int sb = gg & 1;
-        if (!wait(&p_full[sb], (gg >> 1) & 1)) return false;
-        if (first && k >= 1 && !wait(o_empty, (k - 1) & 1)) return false;
-        tc_fence_after();
-        const int st = gg % STAGES;
-        const uint32_t v_base = kv_base + st * L::kStageBytes;
-        const uint32_t pa = p_base + (TILE == 32 ? sb * 64 : sb * 16384);
-#pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk) {
-          const uint64_t ad = make_desc_sw128(pa + kk * 32, 16, 1024);
-          const uint64_t bd = make_desc_sw128(v_base + kk * 2048, L::kChunkBytes, 1024);
-          umma_ss(tmem + kOCol, ad, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
-        }
-        umma_commit(&p_empty[sb]);
-        umma_commit(&kv_empty[st]);
-        return true;
-      };
-      for (int u = cid; u < pp.num_units && ok; u += ncl) {
-        UnitInfo ui = unit_info<TILE>(pp, u);
-        if (ui.ntiles == 0) continue;
-        if (!wait(q_full, k & 1)) { ok = false; break; }
-        const int g0 = g;
-        for (int j = 0; j < ui.ntiles; ++j, ++g) {
-          const int st = g % STAGES;
-          const int sb = g & 1;
-          if (!wait(&kv_full[st], (g / STAGES) & 1)) { ok = false; break; }
-          if (g >= 2 && !wait(&s_empty[sb], ((g >> 1) - 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t kv_st = kv_base + st * L::kStageBytes;
-          for (int c = 0; c < nch; ++c) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = make_desc_sw128(q_base + c * 16384 + kk * 32, 16, 1024);
-              const uint64_t bd = make_desc_sw128(kv_st + c * L::kChunkBytes + kk * 32, 16, 1024);
-              umma_ss(tmem + kSCol + sb * TILE, ad, bd, idesc_qk, (c | kk) ? 1u : 0u);
+      int row_cur = 0;
+      if (it.valid && lane < nbox) row_cur = box_row(it.ui, it.ui.lo, lane);
+      while (it.valid) {
+        const UnitInfo ui = it.ui;
+        const int t0 = ui.lo + it.j * TILE;
+        TileIter<TILE> nx = it;
+        nx.advance(pp);
+        int row_next = 0;
+        if (nx.valid && lane < nbox) row_next = box_row(nx.ui, nx.ui.lo + nx.j * TILE, lane);
+        if (it.first() && it.newq) {
+          if (lane == 0) {
+            if (it.nq >= 1 && !wait(&bar[B_Q_EMPTY], (it.nq - 1) & 1)) ok = false;
+            if (ok) {
+              mbar_arrive_expect_tx(&bar[B_QR_FULL], 16384);
+              tma_load_2d(sQr, &tm_qpe, &bar[B_QR_FULL], 0, (ui.b * pp.q_len + ui.i) * pp.H, pol_q);
+              ++qloads;
             }
           }
-          umma_commit(&s_full[sb]);
-          if (j == ui.ntiles - 1) umma_commit(q_empty);
-          if (j >= 1 && !issue_pv(g - 1, j - 1 == 0)) { ok = false; break; }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+        }
+        const CUtensorMap* map = ui.current ? &tm_cur : &tm_kv;
+        for (int c = 0; c < 9; ++c) {
+          const int st = cs % L::kNK;
+          if (lane == 0 && cs >= L::kNK && !wait(&bar[B_KEMPTY + st], ((cs / L::kNK) - 1) & 1))
+            ok = false;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (lane == 0) mbar_arrive_expect_tx(&bar[B_KFULL + st], L::kKStage);
+          for (int l = 0; l < nbox; ++l) {
+            const int row = __shfl_sync(0xffffffffu, row_cur, l);
+            if (lane == 0)
+              tma_load_2d(sK + st * L::kKStage + l * pp.box_rows * 128, map, &bar[B_KFULL + st],
+                          c * 64, row, pol_kv);
+          }
+          last_cs[st] = cs;
+          ++cs;
         }
         if (!ok) break;
-        if (!issue_pv(g - 1, ui.ntiles == 1)) { ok = false; break; }
-        (void)g0;
-        ++k;
+        (void)t0;
+        row_cur = row_next;
+        it = nx;
       }
-      // drain: all MMAs of this thread complete before TMEM is released
-      umma_commit(mma_done);
-      mbar_wait(mma_done, 0, err);
-    }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax
-    const int r = threadIdx.x - 128;             // TMEM lane == query head
-    const int wq = warp & 3;                     // TMEM lane quarter of this warp
-    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t x_peer = map_to_peer(sX, peer);
-    const uint32_t xfull_peer0 = map_to_peer(&x_full[0], peer);
-    const uint32_t xempty_peer0 = map_to_peer(&x_empty[0], peer);
-    uint8_t* my_x = sX;
-    int g = 0, k = 0;
-    bool ok = true;
-    for (int u = cid; u < pp.num_units && ok; u += ncl) {
-      UnitInfo ui = unit_info<TILE>(pp, u);
-      const int64_t row_out =
-          (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H + r;
-      if (ui.ntiles == 0) {
-        // empty part: o = 0, lse = -inf
-        if (r < pp.H) {
-          for (int c = 0; c < 256; c += 8) {
-            const int64_t e = row_out * 512 + rank * 256 + c;
-            if (pp.part_dtype == 2) {
-              float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-              reinterpret_cast<float4*>(static_cast<float*>(pp.o_part) + e)[0] = z;
-              reinterpret_cast<float4*>(static_cast<float*>(pp.o_part) + e)[1] = z;
-            } else {
-              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(pp.o_part) + e) =
-                  make_uint4(0, 0, 0, 0);
+      if (lane == 0) {
+        for (int s = 0; s < L::kNK; ++s)
+          if (last_cs[s] >= 0) mbar_wait(&bar[B_KFULL + s], (last_cs[s] / L::kNK) & 1, err);
+        if (qloads > 0) mbar_wait(&bar[B_QR_FULL], (qloads - 1) & 1, err);
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------ rank 0: MMA issuer (QK)
+      if (lane == 0) {
+        constexpr uint32_t idesc = make_idesc_f16(128, TILE, BF16, false, false);
+        const uint32_t k_base = smem_u32(sK);
+        const uint32_t qr_base = smem_u32(sQr);
+        TileIter<TILE> it;
+        it.start(pp, u0, u1);
+        int g = 0, cs = 0;
+        bool ok = true;
+        while (ok && it.valid) {
+          if (it.first() && it.newq) {
+            if (!wait(&bar[B_QLAT_FULL], it.nq & 1) || !wait(&bar[B_QR_FULL], it.nq & 1)) {
+              ok = false;
+              break;
             }
           }
-          if (rank == 0) pp.lse_part[row_out] = -INFINITY;
+          const int sb = g & 1;
+          if (g >= 2 && !wait(&bar[B_S_EMPTY + sb], ((g >> 1) - 1) & 1)) { ok = false; break; }
+          const uint32_t d = tmem + kSCol + sb * TILE;
+          for (int c = 0; c < 9; ++c) {
+            const int st = cs % L::kNK;
+            if (!wait(&bar[B_KFULL + st], (cs / L::kNK) & 1)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t kb = k_base + st * L::kKStage;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = make_desc_sw128(kb + kk * 32, 16, 1024);
+              if (c < 8)
+                umma_ts(d, tmem + kQlatCol + c * 32 + kk * 8, bd, idesc, (c | kk) ? 1u : 0u);
+              else
+                umma_ss(d, make_desc_sw128(qr_base + kk * 32, 16, 1024), bd, idesc, 1u);
+            }
+            umma_commit(&bar[B_KEMPTY + st]);
+            ++cs;
+          }
+          if (!ok) break;
+          umma_commit(&bar[B_S_FULL + sb]);
+          if (it.last_of_q(pp)) umma_commit(&bar[B_Q_EMPTY]);
+          it.advance(pp);
+          ++g;
         }
-        continue;
+        umma_commit(&bar[B_MMA_DONE_A]);
+        mbar_wait(&bar[B_MMA_DONE_A], 0, err);
       }
-      float m = -INFINITY;   // running max, log2 domain
-      float l = 0.f;         // running sum of exp2(x - m)
-      for (int j = 0; j < ui.ntiles; ++j, ++g) {
+    } else if (warp == 2 || warp == 3) {
+      // ------------------------------------------------ rank 0: LSE of empty parts
+      const int t = threadIdx.x - 64;
+      for (int u = u0; u < u1; ++u) {
+        const UnitInfo ui = unit_info<TILE>(pp, u);
+        if (ui.ntiles != 0) continue;
+        const int64_t row0 = (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H;
+        for (int h = t; h < pp.H; h += 64) pp.lse_part[row0 + h] = -INFINITY;
+      }
+    } else {
+      // ------------------------------------------------ rank 0: softmax
+      const int r = threadIdx.x - 128;           // TMEM lane == head row
+      const int wq = warp & 3;
+      const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+      const uint32_t precv_peer = map_to_peer(smem + L::kPrOff, 1);
+      const uint32_t pfull_peer = map_to_peer(&bar[B_P_FULL], 1);
+      TileIter<TILE> it;
+      it.start(pp, u0, u1);
+      int g = 0;
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      while (ok && it.valid) {
+        const UnitInfo ui = it.ui;
+        if (it.first()) {
+          if (it.newq) {
+            // Q latent row r -> TMEM (packed pairs, low half = even element)
+            if (it.nq >= 1 && !wait(&bar[B_Q_EMPTY], (it.nq - 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+            const uint4* src = reinterpret_cast<const uint4*>(
+                q_abs + (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.H + r) * 512);
+#pragma unroll 1
+            for (int k = 0; k < 8; ++k) {
+              uint32_t w[32];
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                uint4 x = make_uint4(0, 0, 0, 0);
+                if (r < pp.H) x = __ldg(src + k * 8 + v);
+                w[4 * v] = x.x;
+                w[4 * v + 1] = x.y;
+                w[4 * v + 2] = x.z;
+                w[4 * v + 3] = x.w;
+              }
+              tmem_st32(tmem + lane_base + kQlatCol + k * 32, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_QLAT_FULL]);
+          }
+          m = -INFINITY;
+          l = 0.f;
+        }
         const int sb = g & 1;
-        const int nvalid = min(TILE, ui.hi - (ui.lo + j * TILE));
-        if (!wait(&s_full[sb], (g >> 1) & 1)) { ok = false; break; }
+        if (!wait(&bar[B_S_FULL + sb], (g >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         float s[TILE];
 #pragma unroll
@@ -363,121 +454,272 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[sb]);
+        if (lane == 0) mbar_arrive(&bar[B_S_EMPTY + sb]);
 
-        // ---- swap partial S with the peer CTA (fp32, swizzled rows)
-        if (g >= 2 && !wait_cl(&x_empty[sb], ((g >> 1) - 1) & 1)) { ok = false; break; }
-        const uint32_t xrow_peer = x_peer + sb * L::kXBytes + r * (TILE * 4);
-#pragma unroll
-        for (int uu = 0; uu < TILE / 4; ++uu)
-          st_cluster_v4(xrow_peer + ((uu ^ (r & 7)) << 4), s[4 * uu], s[4 * uu + 1],
-                        s[4 * uu + 2], s[4 * uu + 3]);
-        __syncwarp();
-        if (lane == 0) {
-          fence_acq_rel_cluster();
-          mbar_arrive_remote(xfull_peer0 + sb * 8);
-        }
-        if (!wait_cl(&x_full[sb], (g >> 1) & 1)) { ok = false; break; }
-        const uint8_t* xrow = my_x + sb * L::kXBytes + r * (TILE * 4);
-#pragma unroll
-        for (int uu = 0; uu < TILE / 4; ++uu) {
-          const float4 o4 = *reinterpret_cast<const float4*>(xrow + ((uu ^ (r & 7)) << 4));
-          s[4 * uu] += o4.x;
-          s[4 * uu + 1] += o4.y;
-          s[4 * uu + 2] += o4.z;
-          s[4 * uu + 3] += o4.w;
-        }
-        __syncwarp();
-        if (lane == 0) {
-          fence_acq_rel_cluster();
-          mbar_arrive_remote(xempty_peer0 + sb * 8);
-        }
-
-        // ---- online softmax (log2 domain)
-        float mt = -INFINITY;
+        // ---- online softmax in the log2 domain
+        const int nvalid = min(TILE, ui.hi - (ui.lo + it.j * TILE));
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int t = 0; t < TILE; ++t) {
-          bool valid = t < nvalid;
-          if (ui.current) valid = t <= ui.i;
-          s[t] = valid ? s[t] * pp.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, s[t]);
+          s[t] = t < nvalid ? s[t] * pp.scale_log2 : -INFINITY;
+          mx[t & 3] = fmaxf(mx[t & 3], s[t]);
         }
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         bool need_rescale = false;
         float alpha = 1.f;
-        if (j == 0) {
+        if (it.first()) {
           m = mt;
         } else if (mt > m + kRescaleThresh) {
           need_rescale = true;
           alpha = fast_exp2(m - mt);
           m = mt;
         }
-        float psum = 0.f;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int t = 0; t < TILE; ++t) {
-          s[t] = fast_exp2(s[t] - m);   // masked: exp2(-inf) = 0
-          psum += s[t];
+          s[t] = fast_exp2(s[t] - m);     // masked: exp2(-inf) = 0
+          ps[t & 3] += s[t];
         }
-        l = l * alpha + psum;
+        l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
 
-        // O rescale (rare): needs PV of the previous tile complete
-        if (__any_sync(0xffffffffu, need_rescale)) {
-          if (!wait(&p_empty[(g - 1) & 1], ((g - 1) >> 1) & 1)) { ok = false; break; }
+        // ---- P message for rank 1
+        uint8_t* msg = sPs + sb * L::kMsgStride;
+        if (threadIdx.x == 128) bulk_wait_read<1>();   // copy of tile g-2 has read msg
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int uu = 0; uu < 8; ++uu) {
+            const int t = half * 64 + uu * 8;
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = pack2<BF16>(s[t + 2 * e], s[t + 2 * e + 1]);
+            *reinterpret_cast<uint4*>(msg + half * 16384 + sw128_offset(r, uu)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        reinterpret_cast<float*>(msg + L::kMsgAlpha)[r] = alpha;
+        reinterpret_cast<float*>(msg + L::kMsgL)[r] = l;
+        const uint32_t any = __any_sync(0xffffffffu, need_rescale) ? 1u : 0u;
+        if (lane == 0) warp_flags[wq] = any;
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 128) {
+          const uint32_t flags = (warp_flags[0] | warp_flags[1] | warp_flags[2] | warp_flags[3]) |
+                                 (it.last() ? 2u : 0u);
+          *reinterpret_cast<volatile uint32_t*>(msg + L::kMsgHdr) = flags;
+          fence_proxy_async_smem();
+          if (g >= 2 && !wait_cl(&bar[B_PFREE + sb], ((g >> 1) - 1) & 1)) ok = false;
+          if (ok) {
+            bulk_copy_to_peer(precv_peer + sb * L::kMsgStride, msg, L::kMsgBytes,
+                              pfull_peer + sb * 8);
+            bulk_commit();
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
+        if (it.last() && r < pp.H) {
+          const int64_t row_out =
+              (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H + r;
+          pp.lse_part[row_out] = (m + __log2f(l)) * 0.6931471805599453f;
+        }
+        it.advance(pp);
+        ++g;
+      }
+      if (threadIdx.x == 128) bulk_wait_read<0>();
+    }
+  } else {
+    uint8_t* sV = smem + L::kVOff;
+    uint8_t* sPr = smem + L::kPrOff;
+    if (warp == 0) {
+      // ------------------------------------------------ rank 1: TMA producer (V)
+      const uint64_t pol_kv = policy_evict_first();    // second and last reader
+      TileIter<TILE> it;
+      it.start(pp, u0, u1);
+      int vs = 0;
+      int last_vs[L::kNV];
+#pragma unroll
+      for (int s = 0; s < L::kNV; ++s) last_vs[s] = -1;
+      bool ok = true;
+      int row_cur = 0;
+      if (it.valid && lane < nbox) row_cur = box_row(it.ui, it.ui.lo, lane);
+      const int sub_boxes = L::kVSub / pp.box_rows;   // boxes per 32-token stage (1 or 2)
+      while (it.valid) {
+        const UnitInfo ui = it.ui;
+        TileIter<TILE> nx = it;
+        nx.advance(pp);
+        int row_next = 0;
+        if (nx.valid && lane < nbox) row_next = box_row(nx.ui, nx.ui.lo + nx.j * TILE, lane);
+        const CUtensorMap* map = ui.current ? &tm_cur : &tm_kv;
+        for (int sub = 0; sub < TILE / L::kVSub; ++sub) {
+          const int st = vs % L::kNV;
+          if (lane == 0 && vs >= L::kNV && !wait(&bar[B_VEMPTY + st], ((vs / L::kNV) - 1) & 1))
+            ok = false;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (lane == 0) mbar_arrive_expect_tx(&bar[B_VFULL + st], L::kVStage);
+          for (int bb = 0; bb < sub_boxes; ++bb) {
+            const int row = __shfl_sync(0xffffffffu, row_cur, sub * sub_boxes + bb);
+            if (lane == 0) {
+              for (int c = 0; c < 8; ++c)
+                tma_load_2d(sV + st * L::kVStage + c * L::kVChunk + bb * pp.box_rows * 128, map,
+                            &bar[B_VFULL + st], c * 64, row, pol_kv);
+            }
+          }
+          last_vs[st] = vs;
+          ++vs;
+        }
+        if (!ok) break;
+        row_cur = row_next;
+        it = nx;
+      }
+      if (lane == 0)
+        for (int s = 0; s < L::kNV; ++s)
+          if (last_vs[s] >= 0) mbar_wait(&bar[B_VFULL + s], (last_vs[s] / L::kNV) & 1, err);
+    } else if (warp == 1) {
+      // ------------------------------------------------ rank 1: MMA issuer (PV)
+      if (lane == 0) {
+        constexpr uint32_t idesc = make_idesc_f16(128, 256, BF16, false, true);
+        const uint32_t v_base = smem_u32(sV);
+        const uint32_t p_base = smem_u32(sPr);
+        TileIter<TILE> it;
+        it.start(pp, u0, u1);
+        int g = 0, vs = 0, nfix = 0;
+        bool ok = true;
+        while (ok && it.valid) {
+          const int sb = g & 1;
+          if (!wait(&bar[B_P_FULL + sb], (g >> 1) & 1)) { ok = false; break; }
+          const uint32_t hdr =
+              *reinterpret_cast<volatile uint32_t*>(sPr + sb * L::kMsgStride + L::kMsgHdr);
+          const bool first = it.first();
+          if (first && it.k >= 1 && !wait(&bar[B_O_EMPTY], (it.k - 1) & 1)) { ok = false; break; }
+          if (hdr & 1u) {
+            if (!wait(&bar[B_O_FIXED], nfix & 1)) { ok = false; break; }
+            ++nfix;
+          }
+          const uint32_t pa = p_base + sb * L::kMsgStride;
+          for (int sub = 0; sub < TILE / L::kVSub; ++sub) {
+            const int st = vs % L::kNV;
+            if (!wait(&bar[B_VFULL + st], (vs / L::kNV) & 1)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t vb = v_base + st * L::kVStage;
+#pragma unroll
+            for (int kk = 0; kk < L::kVSub / 16; ++kk) {
+              const int tok = sub * L::kVSub + kk * 16;
+              const uint64_t ad = make_desc_sw128(pa + (tok >> 6) * 16384 + (tok & 63) * 2, 16, 1024);
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const uint64_t bd =
+                    make_desc_sw128(vb + half * 4 * L::kVChunk + kk * 2048, L::kVChunk, 1024);
+                umma_ss(tmem + half * 256, ad, bd, idesc, (first && sub == 0 && kk == 0) ? 0u : 1u);
+              }
+            }
+            umma_commit(&bar[B_VEMPTY + st]);
+            ++vs;
+          }
+          if (!ok) break;
+          umma_commit(&bar[B_PV_DONE + sb]);
+          it.advance(pp);
+          ++g;
+        }
+        umma_commit(&bar[B_MMA_DONE_B]);
+        mbar_wait(&bar[B_MMA_DONE_B], 0, err);
+      }
+    } else if (warp == 2) {
+      // ------------------------------------------------ rank 1: hand P buffers back
+      if (lane == 0) {
+        const uint32_t pfree_peer = map_to_peer(&bar[B_PFREE], 0);
+        TileIter<TILE> it;
+        it.start(pp, u0, u1);
+        int g = 0;
+        while (it.valid) {
+          const int sb = g & 1;
+          if (!wait(&bar[B_PV_DONE + sb], (g >> 1) & 1)) break;
+          if (!wait(&bar[B_META_READ + sb], (g >> 1) & 1)) break;
+          mbar_arrive_expect_tx(&bar[B_P_FULL + sb], L::kMsgBytes);   // tile g + 2
+          mbar_arrive_remote(pfree_peer + sb * 8);
+          it.advance(pp);
+          ++g;
+        }
+      }
+    } else if (warp == 3) {
+      // ------------------------------------------------ rank 1: zeros of empty parts
+      for (int u = u0; u < u1; ++u) {
+        const UnitInfo ui = unit_info<TILE>(pp, u);
+        if (ui.ntiles != 0) continue;
+        const int64_t row0 = (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H;
+        for (int h = 0; h < pp.H; ++h) {
+          const int64_t e0 = (row0 + h) * 512;
+          if (pp.part_dtype == kFP32) {
+            float4* o = reinterpret_cast<float4*>(static_cast<float*>(pp.o_part) + e0);
+            for (int c = lane; c < 128; c += 32) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+          } else {
+            uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(pp.o_part) + e0);
+            for (int c = lane; c < 64; c += 32) o[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+    } else {
+      // ------------------------------------------------ rank 1: O rescale + epilogue
+      const int r = threadIdx.x - 128;
+      const int wq = warp & 3;
+      const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+      TileIter<TILE> it;
+      it.start(pp, u0, u1);
+      int g = 0;
+      bool ok = true;
+      while (ok && it.valid) {
+        const UnitInfo ui = it.ui;
+        const int sb = g & 1;
+        if (!wait(&bar[B_P_FULL + sb], (g >> 1) & 1)) { ok = false; break; }
+        const uint8_t* msg = sPr + sb * L::kMsgStride;
+        const uint32_t hdr = *reinterpret_cast<const volatile uint32_t*>(msg + L::kMsgHdr);
+        const float alpha = reinterpret_cast<const float*>(msg + L::kMsgAlpha)[r];
+        const float lsum = reinterpret_cast<const float*>(msg + L::kMsgL)[r];
+        if (hdr & 1u) {
+          // O *= alpha before PV of this tile; PV of the previous tile must be done
+          if (!wait(&bar[B_PV_DONE + ((g - 1) & 1)], ((g - 1) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          for (int c0 = 0; c0 < 256; c0 += 32) {
+          for (int c0 = 0; c0 < 512; c0 += 32) {
             uint32_t v[32];
-            tmem_ld32(tmem + lane_base + kOCol + c0, v);
+            tmem_ld32(tmem + lane_base + c0, v);
             tmem_wait_ld();
 #pragma unroll
             for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
-            tmem_st32(tmem + lane_base + kOCol + c0, v);
+            tmem_st32(tmem + lane_base + c0, v);
           }
           tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar[B_O_FIXED]);
         }
-
-        // ---- P (bf16 / fp16, swizzled K-major rows) for the PV MMA
-        if (g >= 2 && !wait(&p_empty[sb], ((g >> 1) - 1) & 1)) { ok = false; break; }
-        uint8_t* prow = sP + (TILE == 32 ? 0 : sb * 16384);
-        const int ubase = TILE == 32 ? sb * 4 : 0;
-#pragma unroll
-        for (int uu = 0; uu < TILE / 8; ++uu) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) w[e] = pack2<BF16>(s[8 * uu + 2 * e], s[8 * uu + 2 * e + 1]);
-          *reinterpret_cast<uint4*>(prow + sw128_offset(r, ubase + uu)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+        if (hdr & 2u) {
+          // epilogue: O / l -> o_part
+          if (!wait(&bar[B_PV_DONE + sb], (g >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const int64_t row_out =
+              (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H + r;
+          const float inv_l = 1.f / lsum;
+          for (int c0 = 0; c0 < 512; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + c0, v);
+            tmem_wait_ld();
+            if (r < pp.H) store_row32(pp.o_part, row_out * 512 + c0, v, inv_l, pp.part_dtype);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar[B_O_EMPTY]);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[sb]);
+        if (lane == 0) mbar_arrive(&bar[B_META_READ + sb]);
+        it.advance(pp);
+        ++g;
       }
-      if (!ok) break;
-
-      // ---- epilogue: O / l -> o_part, lse -> lse_part
-      const int gl = g - 1;
-      if (!wait(&p_empty[gl & 1], (gl >> 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      for (int c0 = 0; c0 < 256; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kOCol + c0, v);
-        tmem_wait_ld();
-        if (r < pp.H) {
-          const int64_t e = row_out * 512 + rank * 256 + c0;
-          store_row32(pp.o_part, e, v, inv_l, pp.part_dtype);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_empty);
-      if (rank == 0 && r < pp.H) pp.lse_part[row_out] = (m + __log2f(l)) * 0.6931471805599453f;
-      ++k;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();   // no remote access into this CTA's smem after this point
+  cluster_sync();   // no DSMEM traffic into either CTA after this point
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
@@ -485,11 +727,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 }
 
 // ---------------------------------------------------------------- launcher
-template <int TILE, int STAGES, bool BF16>
-static int launch_partial_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                            const CUtensorMap& d, const PartialParams& pp, cudaStream_t stream) {
-  auto kern = mla_partial_kernel<TILE, STAGES, BF16>;
-  constexpr int smem = PartialSmem<TILE, STAGES>::kTotal;
+template <bool BF16>
+static int launch_partial_t(const CUtensorMap& qpe, const CUtensorMap& kv, const CUtensorMap& cur,
+                            const uint16_t* q_abs, const PartialParams& pp, cudaStream_t stream) {
+  auto kern = mla_partial_kernel<BF16>;
+  constexpr int smem = PairSmem::kTotal;
   static bool configured = false;
   static int max_clusters = 0;
   if (!configured) {
@@ -515,15 +757,15 @@ static int launch_partial_t(const CUtensorMap& a, const CUtensorMap& b, const CU
     configured = true;
   }
   const int clusters = std::max(1, std::min(pp.num_units, max_clusters));
-  kern<<<dim3(2 * clusters), dim3(256), smem, stream>>>(a, b, c, d, pp);
+  kern<<<dim3(2 * clusters), dim3(256), smem, stream>>>(qpe, kv, cur, q_abs, pp);
   return 0;
 }
 
-int launch_partial(const CUtensorMap& qabs, const CUtensorMap& qpe, const CUtensorMap& kv,
-                   const CUtensorMap& cur, const PartialParams& pp, bool bf16,
-                   cudaStream_t stream) {
-  return bf16 ? launch_partial_t<kPartialTile, 4, true>(qabs, qpe, kv, cur, pp, stream)
-              : launch_partial_t<kPartialTile, 4, false>(qabs, qpe, kv, cur, pp, stream);
+int launch_partial(const CUtensorMap& qpe, const CUtensorMap& kv, const CUtensorMap& cur,
+                   const void* q_abs, const PartialParams& pp, bool bf16, cudaStream_t stream) {
+  const uint16_t* q = static_cast<const uint16_t*>(q_abs);
+  return bf16 ? launch_partial_t<true>(qpe, kv, cur, q, pp, stream)
+              : launch_partial_t<false>(qpe, kv, cur, q, pp, stream);
 }
 
 }  // namespace mla
