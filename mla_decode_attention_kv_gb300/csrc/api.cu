@@ -107,19 +107,23 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
     return MLA_ERR_MISALIGNED;
 
   const bool bf16 = in_dtype == MLA_BF16;
-  const int box_rows = block_size < mla::kPartialBox ? block_size : mla::kPartialBox;
+  const int box_k = block_size < mla::kPartialBoxK ? block_size : mla::kPartialBoxK;
+  const int box_v = block_size < mla::kPartialBoxV ? block_size : mla::kPartialBoxV;
   const uint64_t qrows = static_cast<uint64_t>(B) * q_len * H;
-  CUtensorMap tm_qpe, tm_kv, tm_cur;
+  const uint64_t kv_rows = static_cast<uint64_t>(num_blocks) * block_size;
+  CUtensorMap tm_qpe, tm_kv, tm_cur, tm_kv_v, tm_cur_v;
   if (!make_map(&tm_qpe, q_pe, 64, qrows, 128, 64, 128, bf16) ||
-      !make_map(&tm_kv, kv_cache, 576, static_cast<uint64_t>(num_blocks) * block_size, 1152, 64,
-                box_rows, bf16))
+      !make_map(&tm_kv, kv_cache, 576, kv_rows, 1152, 64, box_k, bf16) ||
+      !make_map(&tm_kv_v, kv_cache, 576, kv_rows, 1152, 64, box_v, bf16))
     return MLA_ERR_CUDA;
   if (kv_cur) {
-    if (!make_map(&tm_cur, kv_cur, 576, static_cast<uint64_t>(B) * q_len, 1152, 64, box_rows,
-                  bf16))
+    const uint64_t cur_rows = static_cast<uint64_t>(B) * q_len;
+    if (!make_map(&tm_cur, kv_cur, 576, cur_rows, 1152, 64, box_k, bf16) ||
+        !make_map(&tm_cur_v, kv_cur, 576, cur_rows, 1152, 64, box_v, bf16))
       return MLA_ERR_CUDA;
   } else {
-    tm_cur = tm_kv;   // never read
+    tm_cur = tm_kv;     // never read
+    tm_cur_v = tm_kv_v;
   }
 
   mla::PartialParams pp;
@@ -140,10 +144,11 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
   const int64_t units = static_cast<int64_t>(B) * q_len * pp.P;
   if (units > INT32_MAX) return MLA_ERR_BAD_SHAPE;
   pp.num_units = static_cast<int>(units);
-  pp.box_rows = box_rows;
+  pp.box_rows = box_k;
+  pp.box_rows_v = box_v;
   pp.scale_log2 = scale * 1.4426950408889634f;
   pp.part_dtype = part_dtype;
-  return launched(mla::launch_partial(tm_qpe, tm_kv, tm_cur, q_abs, pp, bf16,
+  return launched(mla::launch_partial(tm_qpe, tm_kv, tm_cur, tm_kv_v, tm_cur_v, q_abs, pp, bf16,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -24,74 +24,133 @@
 namespace mla {
 
 // ---------------------------------------------------------------- weights
-// Weights of the parts of row (t, h); returns LSE (natural log) and writes
-// the normalised weights (0 for empty parts).  Every lane computes the same
-// values in the same order.
-__device__ __forceinline__ float combine_weights(const float* lse_part, int P, int H, int64_t t,
-                                                 int h, const float* lse_local, float* w) {
+// Normalised weights of the parts of row (t, h), spread over the warp: lane
+// l holds the weights of parts l, l + 32 and l + 64 (zero for empty parts).
+// Part index P (when a local partial is given) is the local one.
+struct RowWeights {
+  float w[3];
+  float lse;
+};
+
+__device__ __forceinline__ RowWeights row_weights(const float* lse_part, int P, int H, int64_t t,
+                                                  int h, const float* lse_local, int lane) {
   const int np = P + (lse_local ? 1 : 0);
+  RowWeights rw;
+  float v[3];
   float mx = -INFINITY;
-  for (int p = 0; p < np; ++p) {
-    const float v = p < P ? lse_part[(t * P + p) * H + h] : lse_local[t * H + h];
-    w[p] = v;
-    mx = fmaxf(mx, v);
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const int p = lane + 32 * k;
+    v[k] = -INFINITY;
+    if (p < np) v[k] = p < P ? __ldg(lse_part + (t * P + p) * H + h) : __ldg(lse_local + t * H + h);
+    mx = fmaxf(mx, v[k]);
   }
-  if (mx == -INFINITY) {
-    for (int p = 0; p < np; ++p) w[p] = 0.f;
-    return -INFINITY;
-  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   float sum = 0.f;
-  for (int p = 0; p < np; ++p) {
-    w[p] = w[p] == -INFINITY ? 0.f : __expf(w[p] - mx);
-    sum += w[p];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    v[k] = (mx == -INFINITY || v[k] == -INFINITY) ? 0.f : __expf(v[k] - mx);
+    sum += v[k];
   }
-  const float inv = 1.f / sum;
-  for (int p = 0; p < np; ++p) w[p] *= inv;
-  return mx + __logf(sum);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+#pragma unroll
+  for (int k = 0; k < 3; ++k) rw.w[k] = v[k] * inv;
+  rw.lse = sum > 0.f ? mx + __logf(sum) : -INFINITY;
+  return rw;
 }
 
-// Accumulate 16 consecutive elements of one partial row into acc.
-__device__ __forceinline__ void accum16(const void* src, int64_t e, int dt, float w,
-                                        float (&acc)[16]) {
-  if (dt == kFP32) {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + e);
+__device__ __forceinline__ float weight_of(const RowWeights& rw, int p) {
+  const float x = p < 32 ? rw.w[0] : (p < 64 ? rw.w[1] : rw.w[2]);
+  return __shfl_sync(0xffffffffu, x, p & 31);
+}
+
+// 16 consecutive elements of one partial row: 64 bytes (fp32) or 32 bytes.
+template <bool F32>
+struct Chunk16 {
+  uint4 v[F32 ? 4 : 2];
+};
+
+template <bool F32>
+__device__ __forceinline__ Chunk16<F32> load16(const void* src, int64_t e) {
+  Chunk16<F32> x;
+  const uint4* p = F32 ? reinterpret_cast<const uint4*>(static_cast<const float*>(src) + e)
+                       : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + e);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 v = __ldg(p + q);
-      acc[4 * q] += w * v.x;
-      acc[4 * q + 1] += w * v.y;
-      acc[4 * q + 2] += w * v.z;
-      acc[4 * q + 3] += w * v.w;
+  for (int i = 0; i < (F32 ? 4 : 2); ++i) x.v[i] = __ldg(p + i);
+  return x;
+}
+
+template <bool F32>
+__device__ __forceinline__ void fma16(const Chunk16<F32>& x, int dt, float w, float (&acc)[16]) {
+  if constexpr (F32) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[4 * i] += w * __uint_as_float(x.v[i].x);
+      acc[4 * i + 1] += w * __uint_as_float(x.v[i].y);
+      acc[4 * i + 2] += w * __uint_as_float(x.v[i].z);
+      acc[4 * i + 3] += w * __uint_as_float(x.v[i].w);
     }
   } else {
-    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + e);
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const uint4 v = __ldg(p + q);
-      const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t u[4] = {x.v[i].x, x.v[i].y, x.v[i].z, x.v[i].w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float2 f = unpack2(ws[k], dt);
-        acc[8 * q + 2 * k] += w * f.x;
-        acc[8 * q + 2 * k + 1] += w * f.y;
+        const float2 f = unpack2(u[k], dt);
+        acc[8 * i + 2 * k] += w * f.x;
+        acc[8 * i + 2 * k + 1] += w * f.y;
       }
     }
   }
 }
 
-// Combine row (t, h) for the 16 latent elements of this lane.
-__device__ __forceinline__ float combine_row16(const void* o_part, const float* lse_part, int P,
-                                               const void* o_local, const float* lse_local,
-                                               int H, int64_t t, int h, int part_dt, int lane,
-                                               float (&acc)[16]) {
-  float w[65];
-  const float lse = combine_weights(lse_part, P, H, t, h, lse_local, w);
+// Combine NR rows (t[0..NR)) of head h for this lane's 16 latent elements.
+// All loads of a batch of parts are issued before any of them is used.
+template <int NR, bool F32>
+__device__ __forceinline__ void combine_rows(const void* o_part, const float* lse_part, int P,
+                                             const void* o_local, const float* lse_local, int H,
+                                             const int64_t (&t)[NR], const bool (&valid)[NR],
+                                             int h, int dt, int lane, float (&acc)[NR][16],
+                                             float (&lse)[NR]) {
+  constexpr int KB = F32 ? 4 : 8;   // parts per batch
+  RowWeights rw[NR];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  for (int p = 0; p < P; ++p)
-    if (w[p] != 0.f) accum16(o_part, ((t * P + p) * H + h) * 512 + lane * 16, part_dt, w[p], acc);
-  if (o_local && w[P] != 0.f) accum16(o_local, (t * H + h) * 512 + lane * 16, part_dt, w[P], acc);
-  return lse;
+  for (int r = 0; r < NR; ++r) {
+    rw[r] = row_weights(lse_part, P, H, valid[r] ? t[r] : 0, h, lse_local, lane);
+    lse[r] = rw[r].lse;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[r][i] = 0.f;
+  }
+  const int np = P + (o_local ? 1 : 0);
+  for (int p0 = 0; p0 < np; p0 += KB) {
+    Chunk16<F32> x[NR][KB];
+    float w[NR][KB];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+#pragma unroll
+      for (int k = 0; k < KB; ++k) {
+        const int p = p0 + k;
+        w[r][k] = p < np ? weight_of(rw[r], p) : 0.f;
+        if (valid[r] && w[r][k] != 0.f) {
+          const void* src = p < P ? o_part : o_local;
+          const int64_t row = p < P ? (t[r] * P + p) * H + h : t[r] * H + h;
+          x[r][k] = load16<F32>(src, row * 512 + lane * 16);
+        } else {
+#pragma unroll
+          for (int i = 0; i < (F32 ? 4 : 2); ++i) x[r][k].v[i] = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+#pragma unroll
+      for (int k = 0; k < KB; ++k)
+        if (w[r][k] != 0.f) fma16<F32>(x[r][k], dt, w[r][k], acc[r]);
+    }
+  }
 }
 
 __device__ __forceinline__ void store16(void* dst, int64_t e, const float (&v)[16], int dt) {
@@ -111,6 +170,7 @@ __device__ __forceinline__ void store16(void* dst, int64_t e, const float (&v)[1
 
 // ---------------------------------------------------------------- combine
 // One warp per (t, h) row; lane l owns latent elements [16l, 16l + 16).
+template <bool F32>
 __global__ void __launch_bounds__(256) mla_combine_kernel(const void* o_part, const float* lse_part,
                                                           int P, const void* o_local,
                                                           const float* lse_local, int T, int H,
@@ -119,13 +179,15 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const void* o_part, co
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= static_cast<int64_t>(T) * H) return;
-  const int64_t t = row / H;
+  const int64_t t[1] = {row / H};
+  const bool valid[1] = {true};
   const int h = static_cast<int>(row % H);
-  float acc[16];
-  const float lse =
-      combine_row16(o_part, lse_part, P, o_local, lse_local, H, t, h, part_dt, lane, acc);
-  store16(o_latent, row * 512 + lane * 16, acc, out_dt);
-  if (lse_out && lane == 0) lse_out[row] = lse;
+  float acc[1][16];
+  float lse[1];
+  combine_rows<1, F32>(o_part, lse_part, P, o_local, lse_local, H, t, valid, h, part_dt, lane, acc,
+                       lse);
+  store16(o_latent, row * 512 + lane * 16, acc[0], out_dt);
+  if (lse_out && lane == 0) lse_out[row] = lse[0];
 }
 
 // ---------------------------------------------------------------- V-up
@@ -136,7 +198,7 @@ constexpr int kVupSmem = kVupWBytes + kVupBBytes + 1024;
 
 // One CTA per head.  COMBINE: B rows come from the LSE combine of the
 // partials; otherwise they are read from o_latent.
-template <bool COMBINE, bool BF16>
+template <bool COMBINE, bool BF16, bool F32>
 __global__ void __launch_bounds__(256, 1)
     mla_vup_kernel(const __grid_constant__ CUtensorMap tm_w, const void* o_part,
                    const float* lse_part, int P, const void* o_local, const float* lse_local,
@@ -181,38 +243,47 @@ __global__ void __launch_bounds__(256, 1)
   for (int t0 = 0; t0 < T && ok; t0 += kVupRows, phase ^= 1) {
     const int nrows = min(kVupRows, T - t0);
     // ---- B operand: rows t0 .. t0 + 63 of head h, latent K-major, SW128
-    for (int rr = warp; rr < kVupRows; rr += 8) {
-      float acc[16];
-      const int64_t t = t0 + rr;
-      if (rr < nrows) {
-        if constexpr (COMBINE) {
-          const float lse = combine_row16(o_part, lse_part, P, o_local, lse_local, H, t, h,
-                                          part_dt, lane, acc);
-          if (o_latent_out) store16(o_latent_out, (t * H + h) * 512 + lane * 16, acc, dt);
-          if (lse_out && lane == 0) lse_out[t * H + h] = lse;
-        } else {
-          const uint4* src = reinterpret_cast<const uint4*>(
-              static_cast<const uint16_t*>(o_latent_in) + (t * H + h) * 512 + lane * 16);
-          const uint4 a = __ldg(src), b = __ldg(src + 1);
-          const int c = lane >> 2;
-          const int u = 2 * (lane & 3);
-          *reinterpret_cast<uint4*>(sB + c * (kVupRows * 128) + sw128_offset(rr, u)) = a;
-          *reinterpret_cast<uint4*>(sB + c * (kVupRows * 128) + sw128_offset(rr, u + 1)) = b;
-          continue;
+    const int c = lane >> 2;          // 64-element chunk of this lane's 16 values
+    const int u = 2 * (lane & 3);     // first 16-byte unit inside the 128-byte row
+    if constexpr (COMBINE) {
+      for (int rr = warp * 2; rr < kVupRows; rr += 16) {
+        const int64_t t[2] = {t0 + rr, t0 + rr + 1};
+        const bool valid[2] = {rr < nrows, rr + 1 < nrows};
+        float acc[2][16];
+        float lse[2];
+        combine_rows<2, F32>(o_part, lse_part, P, o_local, lse_local, H, t, valid, h, part_dt,
+                             lane, acc, lse);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          if (!valid[q]) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[q][i] = 0.f;
+          } else {
+            if (o_latent_out) store16(o_latent_out, (t[q] * H + h) * 512 + lane * 16, acc[q], dt);
+            if (lse_out && lane == 0) lse_out[t[q] * H + h] = lse[q];
+          }
+          uint32_t wv[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) wv[k] = pack2<BF16>(acc[q][2 * k], acc[q][2 * k + 1]);
+          *reinterpret_cast<uint4*>(sB + c * (kVupRows * 128) + sw128_offset(rr + q, u)) =
+              make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          *reinterpret_cast<uint4*>(sB + c * (kVupRows * 128) + sw128_offset(rr + q, u + 1)) =
+              make_uint4(wv[4], wv[5], wv[6], wv[7]);
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
       }
-      const int c = lane >> 2;          // 64-element chunk of this lane's 16 values
-      const int u = 2 * (lane & 3);     // first 16-byte unit inside the 128-byte row
-      uint32_t wv[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) wv[k] = pack2<BF16>(acc[2 * k], acc[2 * k + 1]);
-      *reinterpret_cast<uint4*>(sB + c * (kVupRows * 128) + sw128_offset(rr, u)) =
-          make_uint4(wv[0], wv[1], wv[2], wv[3]);
-      *reinterpret_cast<uint4*>(sB + c * (kVupRows * 128) + sw128_offset(rr, u + 1)) =
-          make_uint4(wv[4], wv[5], wv[6], wv[7]);
+    } else {
+      for (int rr = warp; rr < kVupRows; rr += 8) {
+        uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+        if (rr < nrows) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              static_cast<const uint16_t*>(o_latent_in) +
+              ((t0 + rr) * static_cast<int64_t>(H) + h) * 512 + lane * 16);
+          a = __ldg(src);
+          b = __ldg(src + 1);
+        }
+        *reinterpret_cast<uint4*>(sB + c * (kVupRows * 128) + sw128_offset(rr, u)) = a;
+        *reinterpret_cast<uint4*>(sB + c * (kVupRows * 128) + sw128_offset(rr, u + 1)) = b;
+      }
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -276,17 +347,21 @@ int launch_combine(const void* o_part, const float* lse_part, int P, const void*
                    float* lse_out, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(T) * H;
   const int blocks = static_cast<int>((rows + 7) / 8);
-  mla_combine_kernel<<<blocks, 256, 0, stream>>>(o_part, lse_part, P, o_local, lse_local, T, H,
-                                                 part_dt, out_dt, o_latent, lse_out);
+  if (part_dt == kFP32)
+    mla_combine_kernel<true><<<blocks, 256, 0, stream>>>(o_part, lse_part, P, o_local, lse_local, T,
+                                                         H, part_dt, out_dt, o_latent, lse_out);
+  else
+    mla_combine_kernel<false><<<blocks, 256, 0, stream>>>(o_part, lse_part, P, o_local, lse_local,
+                                                          T, H, part_dt, out_dt, o_latent, lse_out);
   return 0;
 }
 
-template <bool COMBINE, bool BF16>
+template <bool COMBINE, bool BF16, bool F32>
 static int launch_vup_t(const CUtensorMap& tm_w, const void* o_part, const float* lse_part, int P,
                         const void* o_local, const float* lse_local, const void* o_latent_in,
                         int T, int H, int part_dt, void* out, void* o_latent_out, float* lse_out,
                         int* err, cudaStream_t stream) {
-  auto kern = mla_vup_kernel<COMBINE, BF16>;
+  auto kern = mla_vup_kernel<COMBINE, BF16, F32>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kVupSmem) !=
@@ -303,19 +378,17 @@ int launch_vup(const CUtensorMap& tm_w, bool combine, bool bf16, const void* o_p
                const float* lse_part, int P, const void* o_local, const float* lse_local,
                const void* o_latent_in, int T, int H, int part_dt, void* out, void* o_latent_out,
                float* lse_out, int* err, cudaStream_t stream) {
-  if (combine)
-    return bf16 ? launch_vup_t<true, true>(tm_w, o_part, lse_part, P, o_local, lse_local,
-                                           o_latent_in, T, H, part_dt, out, o_latent_out, lse_out,
-                                           err, stream)
-                : launch_vup_t<true, false>(tm_w, o_part, lse_part, P, o_local, lse_local,
-                                            o_latent_in, T, H, part_dt, out, o_latent_out,
-                                            lse_out, err, stream);
-  return bf16 ? launch_vup_t<false, true>(tm_w, o_part, lse_part, P, o_local, lse_local,
-                                          o_latent_in, T, H, part_dt, out, o_latent_out, lse_out,
-                                          err, stream)
-              : launch_vup_t<false, false>(tm_w, o_part, lse_part, P, o_local, lse_local,
-                                           o_latent_in, T, H, part_dt, out, o_latent_out, lse_out,
-                                           err, stream);
+#define MLA_VUP_ARGS tm_w, o_part, lse_part, P, o_local, lse_local, o_latent_in, T, H, part_dt, out, \
+                     o_latent_out, lse_out, err, stream
+  if (!combine)
+    return bf16 ? launch_vup_t<false, true, false>(MLA_VUP_ARGS)
+                : launch_vup_t<false, false, false>(MLA_VUP_ARGS);
+  if (part_dt == kFP32)
+    return bf16 ? launch_vup_t<true, true, true>(MLA_VUP_ARGS)
+                : launch_vup_t<true, false, true>(MLA_VUP_ARGS);
+  return bf16 ? launch_vup_t<true, true, false>(MLA_VUP_ARGS)
+              : launch_vup_t<true, false, false>(MLA_VUP_ARGS);
+#undef MLA_VUP_ARGS
 }
 
 }  // namespace mla

@@ -15,16 +15,20 @@ struct PartialParams {
   int* err;
   int B, q_len, H, num_blocks, bs, max_blocks, S, P, has_cur;
   int num_units;
-  int box_rows;          // rows per TMA box of the KV maps: min(32, block_size)
+  int box_rows;          // rows per TMA box of the QK CTA's KV maps: min(128, block_size)
+  int box_rows_v;        // rows per TMA box of the PV CTA's KV maps: min(32, block_size)
   float scale_log2;      // softmax scale * log2(e)
   int part_dtype;        // 0 bf16, 1 fp16, 2 fp32
 };
 
-// Rows per TMA box of the partial kernel's KV maps: min(kPartialBox, bs).
-constexpr int kPartialBox = 32;
+// Rows per TMA box of the partial kernel's KV maps: min(box, block_size) for
+// the QK CTA (128-token tiles) and the PV CTA (32-token stages).
+constexpr int kPartialBoxK = 128;
+constexpr int kPartialBoxV = 32;
 
 int launch_partial(const CUtensorMap& qpe, const CUtensorMap& kv, const CUtensorMap& cur,
-                   const void* q_abs, const PartialParams& pp, bool bf16, cudaStream_t stream);
+                   const CUtensorMap& kv_v, const CUtensorMap& cur_v, const void* q_abs,
+                   const PartialParams& pp, bool bf16, cudaStream_t stream);
 int launch_combine(const void* o_part, const float* lse_part, int P, const void* o_local,
                    const float* lse_local, int T, int H, int part_dt, int out_dt, void* o_latent,
                    float* lse_out, cudaStream_t stream);

@@ -165,7 +165,9 @@ template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     mla_partial_kernel(const __grid_constant__ CUtensorMap tm_qpe,
                        const __grid_constant__ CUtensorMap tm_kv,
-                       const __grid_constant__ CUtensorMap tm_cur, const uint16_t* __restrict__ q_abs,
+                       const __grid_constant__ CUtensorMap tm_cur,
+                       const __grid_constant__ CUtensorMap tm_kv_v,
+                       const __grid_constant__ CUtensorMap tm_cur_v, const uint16_t* __restrict__ q_abs,
                        const PartialParams pp) {
   using L = PairSmem;
   constexpr int TILE = L::kTile;
@@ -230,17 +232,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     prefetch_tmap(&tm_qpe);
     prefetch_tmap(&tm_kv);
     prefetch_tmap(&tm_cur);
+    prefetch_tmap(&tm_kv_v);
+    prefetch_tmap(&tm_cur_v);
   }
   __syncthreads();
   cluster_sync();   // every barrier of both CTAs is initialised
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // contiguous range of units of this cluster
+  // Contiguous range of units of this cluster, balanced by tile count: the
+  // cluster owns the units whose first tile falls in its equal share of all
+  // tiles (both CTAs of the pair compute the same range).
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(nclusters_x());
-  const int u0 = static_cast<int>(static_cast<int64_t>(cid) * pp.num_units / ncl);
-  const int u1 = static_cast<int>(static_cast<int64_t>(cid + 1) * pp.num_units / ncl);
+  __shared__ int s_scan[256];
+  __shared__ int s_range[3];
+  {
+    const int U = pp.num_units;
+    const int per = (U + 255) / 256;
+    const int a = min(U, static_cast<int>(threadIdx.x) * per);
+    const int e = min(U, a + per);
+    int cnt = 0;
+    for (int u = a; u < e; ++u) cnt += unit_info<TILE>(pp, u).ntiles;
+    s_scan[threadIdx.x] = cnt;
+    if (threadIdx.x == 0) {
+      s_range[0] = U;
+      s_range[1] = -1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int run = 0;
+      for (int i = 0; i < 256; ++i) {
+        const int c = s_scan[i];
+        s_scan[i] = run;
+        run += c;
+      }
+      s_range[2] = run;
+    }
+    __syncthreads();
+    const int64_t total = s_range[2];
+    const int64_t lo = static_cast<int64_t>(cid) * total / ncl;
+    const int64_t hi = cid == ncl - 1 ? INT64_MAX : static_cast<int64_t>(cid + 1) * total / ncl;
+    int run = s_scan[threadIdx.x];
+    for (int u = a; u < e; ++u) {
+      if (run >= lo && run < hi) {
+        atomicMin(&s_range[0], u);
+        atomicMax(&s_range[1], u + 1);
+      }
+      run += unit_info<TILE>(pp, u).ntiles;
+    }
+    __syncthreads();
+  }
+  const int u0 = s_range[1] < 0 ? 0 : s_range[0];
+  const int u1 = s_range[1] < 0 ? 0 : s_range[1];
 
   auto wait = [&](uint64_t* b, uint32_t parity) -> bool {
     for (uint32_t it = 0; it < kSpinLimit; ++it) {
@@ -260,24 +304,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     *abort_flag = 1;
     return false;
   };
-  // Row (in the KV map) of TMA box `l` of the tile starting at token t0 of
-  // the unit; boxes past the unit's end re-read its last box (in bounds,
+  // TMA box `l` (of `br` rows) of the tile starting at token t0 of the unit.
+  // box_fetch only issues the block-table load; box_final, called one tile
+  // later, checks the id and forms the row, so the producer never waits on
+  // that load.  Boxes past the unit's end re-read its last box (in bounds,
   // masked out by the softmax).
-  auto box_row = [&](const UnitInfo& ui, int t0, int l) -> int {
-    if (ui.current) return ui.b * pp.q_len + l * pp.box_rows;
-    int t = t0 + l * pp.box_rows;
-    const bool past = t >= ui.hi;
-    if (past) t = ui.hi - 1;
-    int pb = pp.block_table[static_cast<int64_t>(ui.b) * pp.max_blocks + t / pp.bs];
+  struct BoxRef {
+    int t, pb;
+    bool past, cur;
+  };
+  auto box_fetch = [&](const UnitInfo& ui, int t0, int l, int br) -> BoxRef {
+    BoxRef r;
+    r.cur = ui.current;
+    if (ui.current) {
+      r.t = 0;
+      r.past = false;
+      r.pb = ui.b * pp.q_len + l * br;
+      return r;
+    }
+    int t = t0 + l * br;
+    r.past = t >= ui.hi;
+    if (r.past) t = ui.hi - 1;
+    r.t = t;
+    r.pb = __ldg(pp.block_table + static_cast<int64_t>(ui.b) * pp.max_blocks + t / pp.bs);
+    return r;
+  };
+  auto box_final = [&](const BoxRef& r, int br) -> int {
+    if (r.cur) return r.pb;
+    int pb = r.pb;
     if (pb < 0 || pb >= pp.num_blocks) {
       set_error(err, kDevBadBlockId);
       pb = 0;
     }
-    int row = pb * pp.bs + (t % pp.bs);
-    if (past) row -= row % pp.box_rows;
+    int row = pb * pp.bs + (r.t % pp.bs);
+    if (r.past) row -= row % br;
     return row;
   };
-  const int nbox = TILE / pp.box_rows;    // TMA boxes per tile and chunk (4 or 8)
+  const int br_k = pp.box_rows;           // rank 0 box rows: min(128, bs)
+  const int br_v = pp.box_rows_v;         // rank 1 box rows: min(32, bs)
 
   if (rank == 0) {
     uint8_t* sK = smem + L::kKOff;
@@ -295,15 +359,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       for (int s = 0; s < L::kNK; ++s) last_cs[s] = -1;
       int qloads = 0;
       bool ok = true;
-      int row_cur = 0;
-      if (it.valid && lane < nbox) row_cur = box_row(it.ui, it.ui.lo, lane);
+      const int nbox = TILE / br_k;      // boxes per chunk of a tile (1, 2 or 8)
+      BoxRef ref_cur{0, 0, false, false};
+      if (it.valid && lane < nbox) ref_cur = box_fetch(it.ui, it.ui.lo, lane, br_k);
       while (it.valid) {
         const UnitInfo ui = it.ui;
         const int t0 = ui.lo + it.j * TILE;
         TileIter<TILE> nx = it;
         nx.advance(pp);
-        int row_next = 0;
-        if (nx.valid && lane < nbox) row_next = box_row(nx.ui, nx.ui.lo + nx.j * TILE, lane);
+        BoxRef ref_next{0, 0, false, false};
+        if (nx.valid && lane < nbox) ref_next = box_fetch(nx.ui, nx.ui.lo + nx.j * TILE, lane, br_k);
+        const int row_cur = lane < nbox ? box_final(ref_cur, br_k) : 0;
         if (it.first() && it.newq) {
           if (lane == 0) {
             if (it.nq >= 1 && !wait(&bar[B_Q_EMPTY], (it.nq - 1) & 1)) ok = false;
@@ -327,7 +393,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           for (int l = 0; l < nbox; ++l) {
             const int row = __shfl_sync(0xffffffffu, row_cur, l);
             if (lane == 0)
-              tma_load_2d(sK + st * L::kKStage + l * pp.box_rows * 128, map, &bar[B_KFULL + st],
+              tma_load_2d(sK + st * L::kKStage + l * br_k * 128, map, &bar[B_KFULL + st],
                           c * 64, row, pol_kv);
           }
           last_cs[st] = cs;
@@ -335,7 +401,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         }
         if (!ok) break;
         (void)t0;
-        row_cur = row_next;
+        ref_cur = ref_next;
         it = nx;
       }
       if (lane == 0) {
@@ -540,16 +606,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 #pragma unroll
       for (int s = 0; s < L::kNV; ++s) last_vs[s] = -1;
       bool ok = true;
-      int row_cur = 0;
-      if (it.valid && lane < nbox) row_cur = box_row(it.ui, it.ui.lo, lane);
-      const int sub_boxes = L::kVSub / pp.box_rows;   // boxes per 32-token stage (1 or 2)
+      const int nbox = TILE / br_v;           // boxes per tile (4 or 8)
+      const int sub_boxes = L::kVSub / br_v;  // boxes per 32-token stage (1 or 2)
+      BoxRef ref_cur{0, 0, false, false};
+      if (it.valid && lane < nbox) ref_cur = box_fetch(it.ui, it.ui.lo, lane, br_v);
       while (it.valid) {
         const UnitInfo ui = it.ui;
         TileIter<TILE> nx = it;
         nx.advance(pp);
-        int row_next = 0;
-        if (nx.valid && lane < nbox) row_next = box_row(nx.ui, nx.ui.lo + nx.j * TILE, lane);
-        const CUtensorMap* map = ui.current ? &tm_cur : &tm_kv;
+        BoxRef ref_next{0, 0, false, false};
+        if (nx.valid && lane < nbox) ref_next = box_fetch(nx.ui, nx.ui.lo + nx.j * TILE, lane, br_v);
+        const int row_cur = lane < nbox ? box_final(ref_cur, br_v) : 0;
+        const CUtensorMap* map = ui.current ? &tm_cur_v : &tm_kv_v;
         for (int sub = 0; sub < TILE / L::kVSub; ++sub) {
           const int st = vs % L::kNV;
           if (lane == 0 && vs >= L::kNV && !wait(&bar[B_VEMPTY + st], ((vs / L::kNV) - 1) & 1))
@@ -561,7 +629,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             const int row = __shfl_sync(0xffffffffu, row_cur, sub * sub_boxes + bb);
             if (lane == 0) {
               for (int c = 0; c < 8; ++c)
-                tma_load_2d(sV + st * L::kVStage + c * L::kVChunk + bb * pp.box_rows * 128, map,
+                tma_load_2d(sV + st * L::kVStage + c * L::kVChunk + bb * br_v * 128, map,
                             &bar[B_VFULL + st], c * 64, row, pol_kv);
             }
           }
@@ -569,7 +637,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           ++vs;
         }
         if (!ok) break;
-        row_cur = row_next;
+        ref_cur = ref_next;
         it = nx;
       }
       if (lane == 0)
@@ -729,6 +797,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 // ---------------------------------------------------------------- launcher
 template <bool BF16>
 static int launch_partial_t(const CUtensorMap& qpe, const CUtensorMap& kv, const CUtensorMap& cur,
+                            const CUtensorMap& kv_v, const CUtensorMap& cur_v,
                             const uint16_t* q_abs, const PartialParams& pp, cudaStream_t stream) {
   auto kern = mla_partial_kernel<BF16>;
   constexpr int smem = PairSmem::kTotal;
@@ -757,15 +826,16 @@ static int launch_partial_t(const CUtensorMap& qpe, const CUtensorMap& kv, const
     configured = true;
   }
   const int clusters = std::max(1, std::min(pp.num_units, max_clusters));
-  kern<<<dim3(2 * clusters), dim3(256), smem, stream>>>(qpe, kv, cur, q_abs, pp);
+  kern<<<dim3(2 * clusters), dim3(256), smem, stream>>>(qpe, kv, cur, kv_v, cur_v, q_abs, pp);
   return 0;
 }
 
 int launch_partial(const CUtensorMap& qpe, const CUtensorMap& kv, const CUtensorMap& cur,
-                   const void* q_abs, const PartialParams& pp, bool bf16, cudaStream_t stream) {
+                   const CUtensorMap& kv_v, const CUtensorMap& cur_v, const void* q_abs,
+                   const PartialParams& pp, bool bf16, cudaStream_t stream) {
   const uint16_t* q = static_cast<const uint16_t*>(q_abs);
-  return bf16 ? launch_partial_t<true>(qpe, kv, cur, q, pp, stream)
-              : launch_partial_t<false>(qpe, kv, cur, q, pp, stream);
+  return bf16 ? launch_partial_t<true>(qpe, kv, cur, kv_v, cur_v, q, pp, stream)
+              : launch_partial_t<false>(qpe, kv, cur, kv_v, cur_v, q, pp, stream);
 }
 
 }  // namespace mla
