@@ -510,13 +510,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         if (!wait(&bar[B_S_FULL + sb], (g >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         float s[TILE];
-#pragma unroll
-        for (int c0 = 0; c0 < TILE; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + kSCol + sb * TILE + c0, v);
+        {
+          // four loads in flight, one wait
+          uint32_t v0[32], v1[32], v2[32], v3[32];
+          const uint32_t sa = tmem + lane_base + kSCol + sb * TILE;
+          tmem_ld32(sa, v0);
+          tmem_ld32(sa + 32, v1);
+          tmem_ld32(sa + 64, v2);
+          tmem_ld32(sa + 96, v3);
           tmem_wait_ld();
 #pragma unroll
-          for (int t = 0; t < 32; ++t) s[c0 + t] = __uint_as_float(v[t]);
+          for (int t = 0; t < 32; ++t) {
+            s[t] = __uint_as_float(v0[t]);
+            s[32 + t] = __uint_as_float(v1[t]);
+            s[64 + t] = __uint_as_float(v2[t]);
+            s[96 + t] = __uint_as_float(v3[t]);
+          }
         }
         tc_fence_before();
         __syncwarp();
