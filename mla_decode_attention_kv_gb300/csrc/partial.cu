@@ -127,7 +127,7 @@ struct TileIter {
 struct PairSmem {
   static constexpr int kTile = 128;
   static constexpr int kKStage = kTile * 128;          // one 64-dim chunk of a tile
-  static constexpr int kNK = 8;
+  static constexpr int kNK = 10;
   static constexpr int kVSub = 32;                     // tokens per V stage
   static constexpr int kVChunk = kVSub * 128;          // one 64-dim chunk of a V stage
   static constexpr int kVStage = 8 * kVChunk;          // 32 tokens x 512 latent
@@ -142,12 +142,12 @@ struct PairSmem {
   static constexpr int kMsgStride = 34816;             // 1024-aligned slot
   // rank 0
   static constexpr int kKOff = 0;
-  static constexpr int kQrOff = kKOff + kNK * kKStage;       // 131072
-  static constexpr int kPsOff = kQrOff + 16384;              // 147456
+  static constexpr int kQrOff = kKOff + kNK * kKStage;       // 163840
+  static constexpr int kPsOff = kQrOff + 16384;              // 180224 (one outgoing message)
   // rank 1
   static constexpr int kVOff = 0;
   static constexpr int kPrOff = kVOff + kNV * kVStage;       // 131072
-  static constexpr int kBarOff = kPsOff + 2 * kMsgStride;    // 217088
+  static constexpr int kBarOff = kPsOff + kMsgStride;        // 215040
   static constexpr int kTotal = kBarOff + 512 + 1024;
 };
 static_assert(PairSmem::kPrOff + 2 * PairSmem::kMsgStride <= PairSmem::kBarOff, "rank-1 plan");
@@ -155,10 +155,10 @@ static_assert(PairSmem::kTotal <= 232448, "shared memory budget");
 
 // Barrier slots in the common block.
 enum : int {
-  B_KFULL = 0, B_KEMPTY = 8, B_QR_FULL = 16, B_Q_EMPTY = 17, B_QLAT_FULL = 18, B_S_FULL = 19,
-  B_S_EMPTY = 21, B_PFREE = 23, B_MMA_DONE_A = 25,
-  B_VFULL = 26, B_VEMPTY = 30, B_P_FULL = 34, B_PV_DONE = 36, B_META_READ = 38, B_O_EMPTY = 40,
-  B_O_FIXED = 41, B_MMA_DONE_B = 42, B_COUNT = 43
+  B_KFULL = 0, B_KEMPTY = 10, B_QR_FULL = 20, B_Q_EMPTY = 21, B_QLAT_FULL = 22, B_S_FULL = 23,
+  B_S_EMPTY = 25, B_PFREE = 27, B_MMA_DONE_A = 29,
+  B_VFULL = 30, B_VEMPTY = 34, B_P_FULL = 38, B_PV_DONE = 40, B_META_READ = 42, B_O_EMPTY = 44,
+  B_O_FIXED = 45, B_MMA_DONE_B = 46, B_COUNT = 47
 };
 
 template <bool BF16>
@@ -484,19 +484,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             tc_fence_after();
             const uint4* src = reinterpret_cast<const uint4*>(
                 q_abs + (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.H + r) * 512);
+            // two passes of 32 independent 16-byte loads (half a row each)
 #pragma unroll 1
-            for (int k = 0; k < 8; ++k) {
-              uint32_t w[32];
+            for (int half = 0; half < 2; ++half) {
+              uint4 x[32];
 #pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                uint4 x = make_uint4(0, 0, 0, 0);
-                if (r < pp.H) x = __ldg(src + k * 8 + v);
-                w[4 * v] = x.x;
-                w[4 * v + 1] = x.y;
-                w[4 * v + 2] = x.z;
-                w[4 * v + 3] = x.w;
+              for (int v = 0; v < 32; ++v)
+                x[v] = r < pp.H ? __ldg(src + half * 32 + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                uint32_t w[32];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                  w[4 * v] = x[k * 8 + v].x;
+                  w[4 * v + 1] = x[k * 8 + v].y;
+                  w[4 * v + 2] = x[k * 8 + v].z;
+                  w[4 * v + 3] = x[k * 8 + v].w;
+                }
+                tmem_st32(tmem + lane_base + kQlatCol + (half * 4 + k) * 32, w);
               }
-              tmem_st32(tmem + lane_base + kQlatCol + k * 32, w);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -558,8 +564,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
 
         // ---- P message for rank 1
-        uint8_t* msg = sPs + sb * L::kMsgStride;
-        if (threadIdx.x == 128) bulk_wait_read<1>();   // copy of tile g-2 has read msg
+        uint8_t* msg = sPs;                           // single outgoing buffer
+        if (threadIdx.x == 128) bulk_wait_read<0>();   // copy of tile g-1 has read msg
         named_bar_sync(1, 128);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
