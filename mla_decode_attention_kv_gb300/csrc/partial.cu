@@ -354,9 +354,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       TileIter<TILE> it;
       it.start(pp, u0, u1);
       int cs = 0;
-      int last_cs[L::kNK];
-#pragma unroll
-      for (int s = 0; s < L::kNK; ++s) last_cs[s] = -1;
       int qloads = 0;
       bool ok = true;
       const int nbox = TILE / br_k;      // boxes per chunk of a tile (1, 2 or 8)
@@ -370,6 +367,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         BoxRef ref_next{0, 0, false, false};
         if (nx.valid && lane < nbox) ref_next = box_fetch(nx.ui, nx.ui.lo + nx.j * TILE, lane, br_k);
         const int row_cur = lane < nbox ? box_final(ref_cur, br_k) : 0;
+        // the tile's box rows, gathered into every lane once per tile
+        int rows[8];
+#pragma unroll
+        for (int l = 0; l < 8; ++l) rows[l] = __shfl_sync(0xffffffffu, row_cur, l);
         if (it.first() && it.newq) {
           if (lane == 0) {
             if (it.nq >= 1 && !wait(&bar[B_Q_EMPTY], (it.nq - 1) & 1)) ok = false;
@@ -383,30 +384,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           if (!ok) break;
         }
         const CUtensorMap* map = ui.current ? &tm_cur : &tm_kv;
-        for (int c = 0; c < 9; ++c) {
-          const int st = cs % L::kNK;
-          if (lane == 0 && cs >= L::kNK && !wait(&bar[B_KEMPTY + st], ((cs / L::kNK) - 1) & 1))
-            ok = false;
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          if (lane == 0) mbar_arrive_expect_tx(&bar[B_KFULL + st], L::kKStage);
-          for (int l = 0; l < nbox; ++l) {
-            const int row = __shfl_sync(0xffffffffu, row_cur, l);
-            if (lane == 0)
-              tma_load_2d(sK + st * L::kKStage + l * br_k * 128, map, &bar[B_KFULL + st],
-                          c * 64, row, pol_kv);
+        // one thread issues the tile's nine chunks; no warp collectives in between
+        if (lane == 0) {
+          for (int c = 0; c < 9; ++c) {
+            const int st = cs % L::kNK;
+            if (cs >= L::kNK && !wait(&bar[B_KEMPTY + st], ((cs / L::kNK) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bar[B_KFULL + st], L::kKStage);
+#pragma unroll
+            for (int l = 0; l < 8; ++l)
+              if (l < nbox)
+                tma_load_2d(sK + st * L::kKStage + l * br_k * 128, map, &bar[B_KFULL + st],
+                            c * 64, rows[l], pol_kv);
+            ++cs;
           }
-          last_cs[st] = cs;
-          ++cs;
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         (void)t0;
         ref_cur = ref_next;
         it = nx;
       }
       if (lane == 0) {
-        for (int s = 0; s < L::kNK; ++s)
-          if (last_cs[s] >= 0) mbar_wait(&bar[B_KFULL + s], (last_cs[s] / L::kNK) & 1, err);
+        // drain: the last chunk issued into each stage has landed
+        for (int s = 0; s < L::kNK && s < cs; ++s) {
+          const int last = cs - 1 - ((cs - 1 - s) % L::kNK);
+          mbar_wait(&bar[B_KFULL + s], (last / L::kNK) & 1, err);
+        }
         if (qloads > 0) mbar_wait(&bar[B_QR_FULL], (qloads - 1) & 1, err);
       }
     } else if (warp == 1) {
@@ -617,9 +623,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       TileIter<TILE> it;
       it.start(pp, u0, u1);
       int vs = 0;
-      int last_vs[L::kNV];
-#pragma unroll
-      for (int s = 0; s < L::kNV; ++s) last_vs[s] = -1;
       bool ok = true;
       const int nbox = TILE / br_v;           // boxes per tile (4 or 8)
       const int sub_boxes = L::kVSub / br_v;  // boxes per 32-token stage (1 or 2)
@@ -632,32 +635,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         BoxRef ref_next{0, 0, false, false};
         if (nx.valid && lane < nbox) ref_next = box_fetch(nx.ui, nx.ui.lo + nx.j * TILE, lane, br_v);
         const int row_cur = lane < nbox ? box_final(ref_cur, br_v) : 0;
+        int rows[8];
+#pragma unroll
+        for (int l = 0; l < 8; ++l) rows[l] = __shfl_sync(0xffffffffu, row_cur, l);
         const CUtensorMap* map = ui.current ? &tm_cur_v : &tm_kv_v;
-        for (int sub = 0; sub < TILE / L::kVSub; ++sub) {
-          const int st = vs % L::kNV;
-          if (lane == 0 && vs >= L::kNV && !wait(&bar[B_VEMPTY + st], ((vs / L::kNV) - 1) & 1))
-            ok = false;
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          if (lane == 0) mbar_arrive_expect_tx(&bar[B_VFULL + st], L::kVStage);
-          for (int bb = 0; bb < sub_boxes; ++bb) {
-            const int row = __shfl_sync(0xffffffffu, row_cur, sub * sub_boxes + bb);
-            if (lane == 0) {
+        if (lane == 0) {
+          for (int sub = 0; sub < TILE / L::kVSub; ++sub) {
+            const int st = vs % L::kNV;
+            if (vs >= L::kNV && !wait(&bar[B_VEMPTY + st], ((vs / L::kNV) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bar[B_VFULL + st], L::kVStage);
+            for (int bb = 0; bb < sub_boxes; ++bb) {
+              int row = rows[0];
+#pragma unroll
+              for (int l = 1; l < 8; ++l)
+                if (l == sub * sub_boxes + bb) row = rows[l];
+#pragma unroll
               for (int c = 0; c < 8; ++c)
                 tma_load_2d(sV + st * L::kVStage + c * L::kVChunk + bb * br_v * 128, map,
                             &bar[B_VFULL + st], c * 64, row, pol_kv);
             }
+            ++vs;
           }
-          last_vs[st] = vs;
-          ++vs;
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         ref_cur = ref_next;
         it = nx;
       }
       if (lane == 0)
-        for (int s = 0; s < L::kNV; ++s)
-          if (last_vs[s] >= 0) mbar_wait(&bar[B_VFULL + s], (last_vs[s] / L::kNV) & 1, err);
+        for (int s = 0; s < L::kNV && s < vs; ++s) {
+          const int last = vs - 1 - ((vs - 1 - s) % L::kNV);
+          mbar_wait(&bar[B_VFULL + s], (last / L::kNV) & 1, err);
+        }
     } else if (warp == 1) {
       // ------------------------------------------------ rank 1: MMA issuer (PV)
       if (lane == 0) {
