@@ -305,39 +305,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     return false;
   };
   // TMA box `l` (of `br` rows) of the tile starting at token t0 of the unit.
-  // box_fetch only issues the block-table load; box_final, called one tile
-  // later, checks the id and forms the row, so the producer never waits on
-  // that load.  Boxes past the unit's end re-read its last box (in bounds,
-  // masked out by the softmax).
-  struct BoxRef {
-    int t, pb;
-    bool past, cur;
+  // Box rows of a tile, one box per lane.  fetch_id only issues the
+  // block-table load of the lane's box (one tile ahead); box_row, called when
+  // that tile is issued, checks the id and forms the row, so the producer
+  // never waits on a table load.  Boxes past the unit's end re-read its last
+  // box (in bounds, masked out by the softmax).
+  const int bs_shift = __ffs(pp.bs) - 1;   // block sizes are powers of two
+  auto fetch_id = [&](const TileIter<TILE>& t, int br, int l) -> int {
+    if (!t.valid || t.ui.current) return 0;
+    const int tk = min(t.ui.lo + t.j * TILE + l * br, t.ui.hi - 1);
+    return __ldg(pp.block_table + static_cast<int64_t>(t.ui.b) * pp.max_blocks + (tk >> bs_shift));
   };
-  auto box_fetch = [&](const UnitInfo& ui, int t0, int l, int br) -> BoxRef {
-    BoxRef r;
-    r.cur = ui.current;
-    if (ui.current) {
-      r.t = 0;
-      r.past = false;
-      r.pb = ui.b * pp.q_len + l * br;
-      return r;
-    }
-    int t = t0 + l * br;
-    r.past = t >= ui.hi;
-    if (r.past) t = ui.hi - 1;
-    r.t = t;
-    r.pb = __ldg(pp.block_table + static_cast<int64_t>(ui.b) * pp.max_blocks + t / pp.bs);
-    return r;
-  };
-  auto box_final = [&](const BoxRef& r, int br) -> int {
-    if (r.cur) return r.pb;
-    int pb = r.pb;
-    if (pb < 0 || pb >= pp.num_blocks) {
+  auto box_row = [&](const TileIter<TILE>& t, int br, int l, int id) -> int {
+    if (t.ui.current) return t.ui.b * pp.q_len + l * br;
+    int tk = t.ui.lo + t.j * TILE + l * br;
+    const bool past = tk >= t.ui.hi;
+    if (past) tk = t.ui.hi - 1;
+    if (id < 0 || id >= pp.num_blocks) {
       set_error(err, kDevBadBlockId);
-      pb = 0;
+      id = 0;
     }
-    int row = pb * pp.bs + (r.t % pp.bs);
-    if (r.past) row -= row % br;
+    int row = (id << bs_shift) + (tk & (pp.bs - 1));
+    if (past) row &= ~(br - 1);
     return row;
   };
   const int br_k = pp.box_rows;           // rank 0 box rows: min(128, bs)
@@ -349,6 +338,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     uint8_t* sPs = smem + L::kPsOff;
     if (warp == 0) {
       // ------------------------------------------------ rank 0: TMA producer
+      // The whole warp runs the loop converged: every lane polls the stage
+      // barrier and lane l issues box l of each chunk (no shuffles, no
+      // divergent single-lane sections on the issue path).
       const uint64_t pol_kv = policy_evict_last();     // rank 1 re-reads the latent
       const uint64_t pol_q = policy_evict_last();
       TileIter<TILE> it;
@@ -357,54 +349,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       int qloads = 0;
       bool ok = true;
       const int nbox = TILE / br_k;      // boxes per chunk of a tile (1, 2 or 8)
-      BoxRef ref_cur{0, 0, false, false};
-      if (it.valid && lane < nbox) ref_cur = box_fetch(it.ui, it.ui.lo, lane, br_k);
+      const bool boxlane = lane < nbox;
+      int id_cur = boxlane ? fetch_id(it, br_k, lane) : 0;
       while (it.valid) {
         const UnitInfo ui = it.ui;
-        const int t0 = ui.lo + it.j * TILE;
         TileIter<TILE> nx = it;
         nx.advance(pp);
-        BoxRef ref_next{0, 0, false, false};
-        if (nx.valid && lane < nbox) ref_next = box_fetch(nx.ui, nx.ui.lo + nx.j * TILE, lane, br_k);
-        const int row_cur = lane < nbox ? box_final(ref_cur, br_k) : 0;
-        // the tile's box rows, gathered into every lane once per tile
-        int rows[8];
-#pragma unroll
-        for (int l = 0; l < 8; ++l) rows[l] = __shfl_sync(0xffffffffu, row_cur, l);
+        const int id_next = boxlane ? fetch_id(nx, br_k, lane) : 0;
+        const int row = boxlane ? box_row(it, br_k, lane, id_cur) : 0;
         if (it.first() && it.newq) {
+          if (it.nq >= 1 && !wait(&bar[B_Q_EMPTY], (it.nq - 1) & 1)) break;
           if (lane == 0) {
-            if (it.nq >= 1 && !wait(&bar[B_Q_EMPTY], (it.nq - 1) & 1)) ok = false;
-            if (ok) {
-              mbar_arrive_expect_tx(&bar[B_QR_FULL], 16384);
-              tma_load_2d(sQr, &tm_qpe, &bar[B_QR_FULL], 0, (ui.b * pp.q_len + ui.i) * pp.H, pol_q);
-              ++qloads;
-            }
+            mbar_arrive_expect_tx(&bar[B_QR_FULL], 16384);
+            tma_load_2d(sQr, &tm_qpe, &bar[B_QR_FULL], 0, (ui.b * pp.q_len + ui.i) * pp.H, pol_q);
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
+          ++qloads;
         }
         const CUtensorMap* map = ui.current ? &tm_cur : &tm_kv;
-        // one thread issues the tile's nine chunks; no warp collectives in between
-        if (lane == 0) {
-          for (int c = 0; c < 9; ++c) {
-            const int st = cs % L::kNK;
-            if (cs >= L::kNK && !wait(&bar[B_KEMPTY + st], ((cs / L::kNK) - 1) & 1)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&bar[B_KFULL + st], L::kKStage);
-#pragma unroll
-            for (int l = 0; l < 8; ++l)
-              if (l < nbox)
-                tma_load_2d(sK + st * L::kKStage + l * br_k * 128, map, &bar[B_KFULL + st],
-                            c * 64, rows[l], pol_kv);
-            ++cs;
+        uint8_t* dst = sK + lane * br_k * 128;
+        for (int c = 0; c < 9; ++c) {
+          const int st = cs % L::kNK;
+          if (cs >= L::kNK && !wait(&bar[B_KEMPTY + st], ((cs / L::kNK) - 1) & 1)) {
+            ok = false;
+            break;
           }
+          if (lane == 0) mbar_arrive_expect_tx(&bar[B_KFULL + st], L::kKStage);
+          if (boxlane)
+            tma_load_2d(dst + st * L::kKStage, map, &bar[B_KFULL + st], c * 64, row, pol_kv);
+          ++cs;
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        (void)t0;
-        ref_cur = ref_next;
+        id_cur = id_next;
         it = nx;
       }
       if (lane == 0) {
@@ -619,6 +594,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     uint8_t* sPr = smem + L::kPrOff;
     if (warp == 0) {
       // ------------------------------------------------ rank 1: TMA producer (V)
+      // Converged warp: lane (bb * 8 + c) issues latent chunk c of box bb of
+      // each 32-token stage; lanes 0..nbox-1 hold the tile's box rows.
       const uint64_t pol_kv = policy_evict_first();    // second and last reader
       TileIter<TILE> it;
       it.start(pp, u0, u1);
@@ -626,43 +603,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       bool ok = true;
       const int nbox = TILE / br_v;           // boxes per tile (4 or 8)
       const int sub_boxes = L::kVSub / br_v;  // boxes per 32-token stage (1 or 2)
-      BoxRef ref_cur{0, 0, false, false};
-      if (it.valid && lane < nbox) ref_cur = box_fetch(it.ui, it.ui.lo, lane, br_v);
+      const int vc = lane & 7, vb = lane >> 3;
+      const bool vlane = vb < sub_boxes;
+      const bool boxlane = lane < nbox;
+      int id_cur = boxlane ? fetch_id(it, br_v, lane) : 0;
       while (it.valid) {
         const UnitInfo ui = it.ui;
         TileIter<TILE> nx = it;
         nx.advance(pp);
-        BoxRef ref_next{0, 0, false, false};
-        if (nx.valid && lane < nbox) ref_next = box_fetch(nx.ui, nx.ui.lo + nx.j * TILE, lane, br_v);
-        const int row_cur = lane < nbox ? box_final(ref_cur, br_v) : 0;
-        int rows[8];
-#pragma unroll
-        for (int l = 0; l < 8; ++l) rows[l] = __shfl_sync(0xffffffffu, row_cur, l);
+        const int id_next = boxlane ? fetch_id(nx, br_v, lane) : 0;
+        const int my_row = boxlane ? box_row(it, br_v, lane, id_cur) : 0;
         const CUtensorMap* map = ui.current ? &tm_cur_v : &tm_kv_v;
-        if (lane == 0) {
-          for (int sub = 0; sub < TILE / L::kVSub; ++sub) {
-            const int st = vs % L::kNV;
-            if (vs >= L::kNV && !wait(&bar[B_VEMPTY + st], ((vs / L::kNV) - 1) & 1)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&bar[B_VFULL + st], L::kVStage);
-            for (int bb = 0; bb < sub_boxes; ++bb) {
-              int row = rows[0];
-#pragma unroll
-              for (int l = 1; l < 8; ++l)
-                if (l == sub * sub_boxes + bb) row = rows[l];
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                tma_load_2d(sV + st * L::kVStage + c * L::kVChunk + bb * br_v * 128, map,
-                            &bar[B_VFULL + st], c * 64, row, pol_kv);
-            }
-            ++vs;
+        uint8_t* dst = sV + vc * L::kVChunk + vb * br_v * 128;
+        for (int sub = 0; sub < TILE / L::kVSub; ++sub) {
+          const int st = vs % L::kNV;
+          const int row = __shfl_sync(0xffffffffu, my_row, (sub * sub_boxes + vb) & 7);
+          if (vs >= L::kNV && !wait(&bar[B_VEMPTY + st], ((vs / L::kNV) - 1) & 1)) {
+            ok = false;
+            break;
           }
+          if (lane == 0) mbar_arrive_expect_tx(&bar[B_VFULL + st], L::kVStage);
+          if (vlane)
+            tma_load_2d(dst + st * L::kVStage, map, &bar[B_VFULL + st], vc * 64, row, pol_kv);
+          ++vs;
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        ref_cur = ref_next;
+        id_cur = id_next;
         it = nx;
       }
       if (lane == 0)
