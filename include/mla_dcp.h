@@ -110,6 +110,17 @@ enum {
  *   o_part     [B, q_len, P, H, 512] part_dtype, P = num_shards + (kv_cur != NULL)
  *   lse_part   [B, q_len, P, H] float32
  *   err_flag   device int32 or NULL (see conventions)
+ *   workspace  device scratch of at least workspace_bytes, or NULL; needs
+ *              no initialisation.  With a workspace the GPU's CTA pairs take
+ *              exactly equal shares of all KV tiles whenever whole shards
+ *              would leave them uneven; a shard cut between pairs has its
+ *              pieces parked there and merged by their LSEs (as in
+ *              mla_lse_combine) into o_part / lse_part by a second kernel on
+ *              the same stream.  Without one each pair takes whole shards.
+ *              Calls that may overlap in time need separate workspaces.
+ *   workspace_bytes  size of workspace; at least
+ *              mla_dcp_decode_partial_workspace_size(B, q_len, num_shards,
+ *              kv_cur != NULL) when workspace != NULL.
  * Returns MLA_OK or an mla_status.
  */
 int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_cache,
@@ -117,7 +128,17 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
                            const void* kv_cur, int B, int q_len, int H, int num_blocks,
                            int block_size, int max_blocks, int num_shards, float scale,
                            int in_dtype, int part_dtype, void* o_part, float* lse_part,
-                           int32_t* err_flag, mla_stream_t stream);
+                           int32_t* err_flag, void* workspace, uint64_t workspace_bytes,
+                           mla_stream_t stream);
+
+/*
+ * mla_dcp_decode_partial_workspace_size -- bytes of workspace that
+ * mla_dcp_decode_partial needs on the current device for these sizes (about
+ * 0.5 MiB per resident CTA pair, plus 4 bytes per (b, i, part)).  Returns 0 if
+ * the sizes are invalid or the device cannot run the kernel.  A library
+ * addition with no counterpart in the sources.
+ */
+uint64_t mla_dcp_decode_partial_workspace_size(int B, int q_len, int num_shards, int has_current);
 
 /*
  * mla_lse_combine -- merge partials by their log-sum-exps.

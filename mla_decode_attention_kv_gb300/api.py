@@ -43,15 +43,40 @@ def _need(t: torch.Tensor, name: str):
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
 
 
+_WORKSPACES = {}
+
+
+def partial_workspace(device, B: int, q_len: int, num_shards: int, has_current: bool):
+    """The default workspace of mla_dcp_decode_partial on `device` (one per
+    device, grown as needed), or None for sizes the library rejects.  Calls
+    that may run at the same time on different streams need workspaces of
+    their own."""
+    device = torch.device(device)
+    with torch.cuda.device(device):
+        need = int(_ffi.lib().mla_dcp_decode_partial_workspace_size(
+            B, q_len, num_shards, 1 if has_current else 0))
+    if need == 0:
+        return None      # invalid sizes: the call itself reports them
+    ws = _WORKSPACES.get(device.index)
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+        _WORKSPACES[device.index] = ws
+    return ws
+
+
 def mla_dcp_decode_partial(q_abs, q_pe, kv_cache, block_table, seq_lens, num_shards: int, *,
                            kv_cur=None, scale: float = DEFAULT_SCALE, part_dtype=None,
-                           o_part=None, lse_part=None, err_flag=None, stream=None):
+                           o_part=None, lse_part=None, err_flag=None, stream=None,
+                           workspace="default"):
     """Partial attention of every (sequence, query token, shard [, CURRENT]).
 
     q_abs [B, q, H, 512], q_pe [B, q, H, 64], kv_cache [num_blocks, bs, 576],
     block_table [B, max_blocks] int32, seq_lens [B] int32 (history lengths),
     kv_cur [B, q, 576] or None.  Returns o_part [B, q, P, H, 512] and
-    lse_part [B, q, P, H] (float32), P = num_shards + (kv_cur is not None)."""
+    lse_part [B, q, P, H] (float32), P = num_shards + (kv_cur is not None).
+    workspace: "default" (the device's shared one), a uint8 CUDA tensor of at
+    least mla_dcp_decode_partial_workspace_size bytes, or None (pairs of CTAs
+    then take whole shards)."""
     B, q_len, H, _ = q_abs.shape
     num_blocks, bs, _ = kv_cache.shape
     P = num_shards + (1 if kv_cur is not None else 0)
@@ -63,11 +88,16 @@ def mla_dcp_decode_partial(q_abs, q_pe, kv_cache, block_table, seq_lens, num_sha
         o_part = torch.empty((B, q_len, P, H, D_LATENT), dtype=part_dtype, device=q_abs.device)
     if lse_part is None:
         lse_part = torch.empty((B, q_len, P, H), dtype=torch.float32, device=q_abs.device)
+    if isinstance(workspace, str):
+        if workspace != "default":
+            raise ValueError("workspace must be 'default', a tensor or None")
+        workspace = partial_workspace(q_abs.device, B, q_len, num_shards, kv_cur is not None)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = _ffi.lib().mla_dcp_decode_partial(
         _p(q_abs), _p(q_pe), _p(kv_cache), _p(block_table), _p(seq_lens), _p(kv_cur),
         B, q_len, H, num_blocks, bs, block_table.shape[1], num_shards, float(scale),
         _code(q_abs.dtype), _code(o_part.dtype), _p(o_part), _p(lse_part), _p(err_flag),
-        _s(stream))
+        _p(workspace), ws_bytes, _s(stream))
     _ffi.check("mla_dcp_decode_partial", st)
     return o_part, lse_part
 
@@ -145,13 +175,13 @@ def mla_gather_kv(kv_cache, block_table, seq_lens, max_len: int, *, dst=None, er
 
 def decode_step(q_abs, q_pe, kv_cache, block_table, seq_lens, W_UV, num_shards: int, *,
                 kv_cur=None, scale: float = DEFAULT_SCALE, part_dtype=None, o_part=None,
-                lse_part=None, out=None, err_flag=None, stream=None):
+                lse_part=None, out=None, err_flag=None, stream=None, workspace="default"):
     """One decode step of the attention layer: partials, then the fused
     combine + V-up.  Returns out [B*q, H*128]."""
     o_part, lse_part = mla_dcp_decode_partial(
         q_abs, q_pe, kv_cache, block_table, seq_lens, num_shards, kv_cur=kv_cur, scale=scale,
         part_dtype=part_dtype, o_part=o_part, lse_part=lse_part, err_flag=err_flag,
-        stream=stream)
+        stream=stream, workspace=workspace)
     return mla_lse_combine_vup(o_part, lse_part, W_UV, out=out, err_flag=err_flag, stream=stream)
 
 

@@ -88,7 +88,8 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
                            const void* kv_cur, int B, int q_len, int H, int num_blocks,
                            int block_size, int max_blocks, int num_shards, float scale,
                            int in_dtype, int part_dtype, void* o_part, float* lse_part,
-                           int32_t* err_flag, mla_stream_t stream) {
+                           int32_t* err_flag, void* workspace, uint64_t workspace_bytes,
+                           mla_stream_t stream) {
   if (!q_abs || !q_pe || !kv_cache || !block_table || !seq_lens || !o_part || !lse_part)
     return MLA_ERR_NULL_POINTER;
   if (!is_half_dtype(in_dtype) || !is_part_dtype(part_dtype)) return MLA_ERR_BAD_DTYPE;
@@ -103,7 +104,8 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
       static_cast<int64_t>(B) * q_len * H > INT32_MAX / 2)
     return MLA_ERR_BAD_SHAPE;
   if (!aligned16(q_abs) || !aligned16(q_pe) || !aligned16(kv_cache) || !aligned16(o_part) ||
-      (kv_cur && !aligned16(kv_cur)) || !aligned16(lse_part))
+      (kv_cur && !aligned16(kv_cur)) || !aligned16(lse_part) ||
+      (workspace && reinterpret_cast<uintptr_t>(workspace) % 256 != 0))
     return MLA_ERR_MISALIGNED;
 
   const bool bf16 = in_dtype == MLA_BF16;
@@ -148,8 +150,32 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
   pp.box_rows_v = box_v;
   pp.scale_log2 = scale * 1.4426950408889634f;
   pp.part_dtype = part_dtype;
+  pp.split = 0;
+  pp.ws_o = nullptr;
+  pp.ws_lse = nullptr;
+  pp.ws_units = nullptr;
+  if (workspace) {
+    const int clusters = mla::partial_max_clusters();
+    if (clusters < 1) return MLA_ERR_CUDA;
+    if (workspace_bytes < mla::partial_workspace_bytes(clusters)) return MLA_ERR_BAD_SHAPE;
+    const size_t recs = (static_cast<size_t>(clusters + 1) * 16 + 255) / 256 * 256;
+    char* w = static_cast<char*>(workspace);
+    pp.split = clusters;
+    pp.ws_units = reinterpret_cast<int4*>(w);
+    pp.ws_lse = reinterpret_cast<float*>(w + recs);
+    pp.ws_o = w + recs + 2 * static_cast<size_t>(clusters) * 128 * 4;
+  }
   return launched(mla::launch_partial(tm_qpe, tm_kv, tm_cur, tm_kv_v, tm_cur_v, q_abs, pp, bf16,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+uint64_t mla_dcp_decode_partial_workspace_size(int B, int q_len, int num_shards, int has_current) {
+  if (B < 1 || q_len < 1 || q_len > 8 || num_shards < 1 || num_shards > MLA_MAX_SHARDS) return 0;
+  const int64_t units = static_cast<int64_t>(B) * q_len * (num_shards + (has_current ? 1 : 0));
+  if (units > INT32_MAX) return 0;
+  const int clusters = mla::partial_max_clusters();
+  if (clusters < 1) return 0;
+  return mla::partial_workspace_bytes(clusters);
 }
 
 int mla_lse_combine(const void* o_part, const float* lse_part, int num_parts, const void* o_local,

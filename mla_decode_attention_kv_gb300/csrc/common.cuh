@@ -60,4 +60,6 @@ __device__ __forceinline__ void store_row32(void* base, int64_t e, const uint32_
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+constexpr float kLn2 = 0.6931471805599453f;
+
 }  // namespace mla

@@ -19,7 +19,23 @@ struct PartialParams {
   int box_rows_v;        // rows per TMA box of the PV CTA's KV maps: min(32, block_size)
   float scale_log2;      // softmax scale * log2(e)
   int part_dtype;        // 0 bf16, 1 fp16, 2 fp32
+  // Split-unit workspace (split = number of CTA pairs, 0 = whole units):
+  // per pair two slots of O / l and LSE (log2, [128]) for the units cut at
+  // the ends of its share, and per pair the record of the split unit whose
+  // last tile it holds (+ one header record), read by the merge kernel.
+  int split;
+  void* ws_o;            // pieces of O / l in the partial dtype, [2*pairs][128][512]
+  float* ws_lse;         // [2*pairs][128]
+  int4* ws_units;        // [pairs + 1]: {unit, first tile, first pair, last pair}; header {T, pairs}
 };
+
+// Workspace of the partial kernel for `clusters` CTA pairs.
+inline size_t partial_workspace_bytes(int clusters) {
+  const size_t slots = 2 * static_cast<size_t>(clusters);
+  const size_t recs = (static_cast<size_t>(clusters + 1) * 16 + 255) / 256 * 256;
+  return recs + slots * 128 * 4 + slots * 512 * 128 * 4;
+}
+int partial_max_clusters();
 
 // Rows per TMA box of the partial kernel's KV maps: min(box, block_size) for
 // the QK CTA (128-token tiles) and the PV CTA (32-token stages).

@@ -35,6 +35,7 @@
 //           w3 zeros of empty parts, w4-7 O rescale + epilogue (thread = row)
 // Every wait is bounded; on timeout the kernel records MLA_DEV_WAIT_TIMEOUT,
 // raises an abort flag, drains its own copies and MMAs, frees TMEM, returns.
+#include <climits>
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -75,43 +76,68 @@ __device__ __forceinline__ UnitInfo unit_info(const PartialParams& pp, int u) {
   return ui;
 }
 
-// Walks the tiles of the non-empty units in [u0, u1) as one flat stream.
+// Tile range of one cluster: tiles [j_begin, ...) of unit u_begin through
+// tiles [..., j_stop) of unit u_last, in the flat order of the units' tiles
+// (global tile index t_begin of the first one).  Units with no tiles whose
+// start falls in the cluster's share are [ue0, ue1).
+struct TileRange {
+  int u_begin, j_begin, u_last, j_stop, t_begin, ue0, ue1;
+};
+
+// Walks the tiles of a TileRange as one flat stream.  A "piece" is the part
+// of one unit inside the range: the whole unit, or (at the ends of the range
+// of a cluster that splits units) a run of its tiles.
 template <int TILE>
 struct TileIter {
-  int u, u_end, j, k, nq, qkey;
+  int u, j, k, nq, qkey;
+  int jfirst, jend;      // tile bounds of the current piece within its unit
+  int ustart;            // global tile index of the unit's first tile
+  int u_last, j_stop;
   bool newq, valid;
   UnitInfo ui;
-  __device__ __forceinline__ void start(const PartialParams& pp, int u0, int u1) {
-    u = u0 - 1;
-    u_end = u1;
+  __device__ __forceinline__ void start(const PartialParams& pp, const TileRange& r) {
+    u_last = r.u_last;
+    j_stop = r.j_stop;
     k = -1;
     nq = -1;
     qkey = -1;
-    valid = true;
-    next_unit(pp);
+    valid = r.u_begin <= r.u_last;
+    if (!valid) return;
+    u = r.u_begin;
+    ui = unit_info<TILE>(pp, u);
+    ustart = r.t_begin - r.j_begin;
+    enter(pp, r.j_begin);
+  }
+  __device__ __forceinline__ void enter(const PartialParams& pp, int j0) {
+    ++k;
+    j = jfirst = j0;
+    jend = u == u_last ? j_stop : ui.ntiles;
+    const int key = ui.b * pp.q_len + ui.i;
+    newq = key != qkey;
+    if (newq) {
+      ++nq;
+      qkey = key;
+    }
   }
   __device__ __forceinline__ void next_unit(const PartialParams& pp) {
-    for (++u; u < u_end; ++u) {
+    while (u < u_last) {
+      ustart += ui.ntiles;
+      ++u;
       ui = unit_info<TILE>(pp, u);
       if (ui.ntiles > 0) {
-        ++k;
-        j = 0;
-        const int key = ui.b * pp.q_len + ui.i;
-        newq = key != qkey;
-        if (newq) {
-          ++nq;
-          qkey = key;
-        }
+        enter(pp, 0);
         return;
       }
     }
     valid = false;
   }
   __device__ __forceinline__ void advance(const PartialParams& pp) {
-    if (++j >= ui.ntiles) next_unit(pp);
+    if (++j >= jend) next_unit(pp);
   }
-  __device__ __forceinline__ bool first() const { return j == 0; }
-  __device__ __forceinline__ bool last() const { return j == ui.ntiles - 1; }
+  __device__ __forceinline__ bool first() const { return j == jfirst; }
+  __device__ __forceinline__ bool last() const { return j == jend - 1; }
+  // Whether the current piece is the whole unit (no other cluster holds tiles of it).
+  __device__ __forceinline__ bool whole() const { return jfirst == 0 && jend == ui.ntiles; }
   // Whether this tile is the last one that reads the current Q.
   __device__ __forceinline__ bool last_of_q(const PartialParams& pp) const {
     if (!last()) return false;
@@ -137,8 +163,9 @@ struct PairSmem {
   static constexpr int kMsgP = 2 * 16384;
   static constexpr int kMsgAlpha = kMsgP;
   static constexpr int kMsgL = kMsgAlpha + 512;
-  static constexpr int kMsgHdr = kMsgL + 512;
-  static constexpr int kMsgBytes = kMsgHdr + 16;       // 33808, multiple of 16
+  static constexpr int kMsgM = kMsgL + 512;
+  static constexpr int kMsgHdr = kMsgM + 512;
+  static constexpr int kMsgBytes = kMsgHdr + 16;       // 34320, multiple of 16
   static constexpr int kMsgStride = 34816;             // 1024-aligned slot
   // rank 0
   static constexpr int kKOff = 0;
@@ -237,16 +264,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   }
   __syncthreads();
   cluster_sync();   // every barrier of both CTAs is initialised
+  griddep_launch_dependents();   // a dependent merge grid may be scheduled as CTAs retire
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Contiguous range of units of this cluster, balanced by tile count: the
-  // cluster owns the units whose first tile falls in its equal share of all
-  // tiles (both CTAs of the pair compute the same range).
+  // Tile share of this cluster: tiles [lo, hi) of the flat order of all
+  // units' tiles, lo = cid * T / ncl.  With a workspace the share is exact
+  // and the units at its ends may be split with the neighbouring clusters
+  // (their pieces are merged through the workspace); without one the cluster
+  // owns the whole units whose first tile falls in its share.  Units without
+  // tiles go to the cluster whose share holds their start.  Both CTAs of the
+  // pair compute the same range.
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(nclusters_x());
   __shared__ int s_scan[256];
-  __shared__ int s_range[3];
+  __shared__ int s_load[256];
+  __shared__ int s_rng[8];
+  TileRange rng;
+  int64_t share_total = 0;
+  bool split = false;
+  // share of pair c: tiles [share_start(c), share_start(c + 1))
+  auto share_start = [&](int c) -> int64_t { return static_cast<int64_t>(c) * share_total / ncl; };
+  auto cluster_of = [&](int64_t t) -> int {   // the pair whose share holds tile t
+    int c = static_cast<int>(t * ncl / share_total);
+    while (c + 1 < ncl && share_start(c + 1) <= t) ++c;
+    while (c > 0 && share_start(c) > t) --c;
+    return c;
+  };
+  auto holds = [&](int c) { return share_start(c + 1) > share_start(c); };
   {
     const int U = pp.num_units;
     const int per = (U + 255) / 256;
@@ -256,9 +301,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     for (int u = a; u < e; ++u) cnt += unit_info<TILE>(pp, u).ntiles;
     s_scan[threadIdx.x] = cnt;
     if (threadIdx.x == 0) {
-      s_range[0] = U;
-      s_range[1] = -1;
+      s_rng[0] = INT_MAX;   // u_begin
+      s_rng[1] = 0;         // j_begin
+      s_rng[2] = -1;        // u_last
+      s_rng[3] = 0;         // j_stop
+      s_rng[4] = U;         // ue0
+      s_rng[5] = U;         // ue1
+      s_rng[7] = 0;         // split
     }
+    for (int c = threadIdx.x; c < ncl; c += 256) s_load[c] = 0;
     __syncthreads();
     if (threadIdx.x == 0) {
       int run = 0;
@@ -267,29 +318,78 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         s_scan[i] = run;
         run += c;
       }
-      s_range[2] = run;
+      s_rng[6] = run;
     }
     __syncthreads();
-    const int64_t total = s_range[2];
-    const int64_t lo = static_cast<int64_t>(cid) * total / ncl;
-    const int64_t hi = cid == ncl - 1 ? INT64_MAX : static_cast<int64_t>(cid + 1) * total / ncl;
-    int run = s_scan[threadIdx.x];
-    for (int u = a; u < e; ++u) {
-      if (run >= lo && run < hi) {
-        atomicMin(&s_range[0], u);
-        atomicMax(&s_range[1], u + 1);
+    share_total = s_rng[6];
+    if (pp.split && share_total > 0) {
+      // Split units only where whole units would leave the busiest pair above
+      // the even share by more than max(2 tiles, 1/8 of the share): the
+      // merge kernel and the extra unit ends cost about that much.
+      int64_t run = s_scan[threadIdx.x];
+      for (int u = a; u < e; ++u) {
+        const int nt = unit_info<TILE>(pp, u).ntiles;
+        if (nt > 0) atomicAdd(&s_load[cluster_of(run)], nt);
+        run += nt;
       }
-      run += unit_info<TILE>(pp, u).ntiles;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int mx = 0;
+        for (int c = 0; c < ncl; ++c) mx = max(mx, s_load[c]);
+        const int64_t even = (share_total + ncl - 1) / ncl;
+        s_rng[7] = mx > even + max(int64_t{2}, even / 8) ? 1 : 0;
+      }
+      __syncthreads();
+      split = s_rng[7] != 0;
+    }
+    const int64_t lo = share_start(cid);
+    const int64_t hi = share_start(cid + 1);
+    int64_t run = s_scan[threadIdx.x];
+    for (int u = a; u < e; ++u) {
+      const int nt = unit_info<TILE>(pp, u).ntiles;
+      if (run >= lo) atomicMin(&s_rng[4], u);
+      if (run >= hi) atomicMin(&s_rng[5], u);
+      if (nt > 0 && lo < hi) {
+        if (split) {
+          if (lo >= run && lo < run + nt) {
+            s_rng[0] = u;
+            s_rng[1] = static_cast<int>(lo - run);
+          }
+          if (hi - 1 >= run && hi - 1 < run + nt) {
+            s_rng[2] = u;
+            s_rng[3] = static_cast<int>(hi - run);
+          }
+        } else if (run >= lo && run < hi) {
+          atomicMin(&s_rng[0], u);
+          atomicMax(&s_rng[2], u);
+        }
+      }
+      run += nt;
     }
     __syncthreads();
+    rng.u_begin = s_rng[0];
+    rng.j_begin = s_rng[1];
+    rng.u_last = s_rng[2];
+    rng.j_stop = split ? s_rng[3] : (rng.u_last >= 0 ? unit_info<TILE>(pp, rng.u_last).ntiles : 0);
+    rng.t_begin = static_cast<int>(lo);
+    rng.ue0 = s_rng[4];
+    rng.ue1 = cid == ncl - 1 ? U : s_rng[5];
   }
-  const int u0 = s_range[1] < 0 ? 0 : s_range[0];
-  const int u1 = s_range[1] < 0 ? 0 : s_range[1];
 
   auto wait = [&](uint64_t* b, uint32_t parity) -> bool {
     for (uint32_t it = 0; it < kSpinLimit; ++it) {
       if (mbar_try_wait(b, parity)) return true;
       if ((it & 1023u) == 1023u && *abort_flag) return false;
+    }
+    set_error(err, kDevWaitTimeout);
+    *abort_flag = 1;
+    return false;
+  };
+  // Waits of whole warp groups off the issue path: polls may suspend.
+  auto wait_lazy = [&](uint64_t* b, uint32_t parity) -> bool {
+    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+      if (mbar_try_wait_sleep(b, parity, kLazyWaitNs)) return true;
+      if ((it & 15u) == 15u && *abort_flag) return false;
     }
     set_error(err, kDevWaitTimeout);
     *abort_flag = 1;
@@ -344,7 +444,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       const uint64_t pol_kv = policy_evict_last();     // rank 1 re-reads the latent
       const uint64_t pol_q = policy_evict_last();
       TileIter<TILE> it;
-      it.start(pp, u0, u1);
+      it.start(pp, rng);
       int cs = 0;
       int qloads = 0;
       bool ok = true;
@@ -397,7 +497,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         const uint32_t k_base = smem_u32(sK);
         const uint32_t qr_base = smem_u32(sQr);
         TileIter<TILE> it;
-        it.start(pp, u0, u1);
+        it.start(pp, rng);
         int g = 0, cs = 0;
         bool ok = true;
         while (ok && it.valid) {
@@ -438,7 +538,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     } else if (warp == 2 || warp == 3) {
       // ------------------------------------------------ rank 0: LSE of empty parts
       const int t = threadIdx.x - 64;
-      for (int u = u0; u < u1; ++u) {
+      for (int u = rng.ue0; u < rng.ue1; ++u) {
         const UnitInfo ui = unit_info<TILE>(pp, u);
         if (ui.ntiles != 0) continue;
         const int64_t row0 = (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H;
@@ -452,7 +552,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       const uint32_t precv_peer = map_to_peer(smem + L::kPrOff, 1);
       const uint32_t pfull_peer = map_to_peer(&bar[B_P_FULL], 1);
       TileIter<TILE> it;
-      it.start(pp, u0, u1);
+      it.start(pp, rng);
       int g = 0;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
@@ -461,7 +561,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         if (it.first()) {
           if (it.newq) {
             // Q latent row r -> TMEM (packed pairs, low half = even element)
-            if (it.nq >= 1 && !wait(&bar[B_Q_EMPTY], (it.nq - 1) & 1)) { ok = false; break; }
+            if (it.nq >= 1 && !wait_lazy(&bar[B_Q_EMPTY], (it.nq - 1) & 1)) { ok = false; break; }
             tc_fence_after();
             const uint4* src = reinterpret_cast<const uint4*>(
                 q_abs + (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.H + r) * 512);
@@ -494,7 +594,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           l = 0.f;
         }
         const int sb = g & 1;
-        if (!wait(&bar[B_S_FULL + sb], (g >> 1) & 1)) { ok = false; break; }
+        if (!wait_lazy(&bar[B_S_FULL + sb], (g >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         float s[TILE];
         {
@@ -562,6 +662,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         }
         reinterpret_cast<float*>(msg + L::kMsgAlpha)[r] = alpha;
         reinterpret_cast<float*>(msg + L::kMsgL)[r] = l;
+        reinterpret_cast<float*>(msg + L::kMsgM)[r] = m;
         const uint32_t any = __any_sync(0xffffffffu, need_rescale) ? 1u : 0u;
         if (lane == 0) warp_flags[wq] = any;
         fence_proxy_async_smem();
@@ -579,11 +680,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
-        if (it.last() && r < pp.H) {
-          const int64_t row_out =
-              (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H + r;
-          pp.lse_part[row_out] = (m + __log2f(l)) * 0.6931471805599453f;
-        }
         it.advance(pp);
         ++g;
       }
@@ -598,7 +694,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       // each 32-token stage; lanes 0..nbox-1 hold the tile's box rows.
       const uint64_t pol_kv = policy_evict_first();    // second and last reader
       TileIter<TILE> it;
-      it.start(pp, u0, u1);
+      it.start(pp, rng);
       int vs = 0;
       bool ok = true;
       const int nbox = TILE / br_v;           // boxes per tile (4 or 8)
@@ -643,7 +739,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         const uint32_t v_base = smem_u32(sV);
         const uint32_t p_base = smem_u32(sPr);
         TileIter<TILE> it;
-        it.start(pp, u0, u1);
+        it.start(pp, rng);
         int g = 0, vs = 0, nfix = 0;
         bool ok = true;
         while (ok && it.valid) {
@@ -690,7 +786,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       if (lane == 0) {
         const uint32_t pfree_peer = map_to_peer(&bar[B_PFREE], 0);
         TileIter<TILE> it;
-        it.start(pp, u0, u1);
+        it.start(pp, rng);
         int g = 0;
         while (it.valid) {
           const int sb = g & 1;
@@ -704,7 +800,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       }
     } else if (warp == 3) {
       // ------------------------------------------------ rank 1: zeros of empty parts
-      for (int u = u0; u < u1; ++u) {
+      for (int u = rng.ue0; u < rng.ue1; ++u) {
         const UnitInfo ui = unit_info<TILE>(pp, u);
         if (ui.ntiles != 0) continue;
         const int64_t row0 = (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H;
@@ -725,20 +821,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       const int wq = warp & 3;
       const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
       TileIter<TILE> it;
-      it.start(pp, u0, u1);
+      it.start(pp, rng);
       int g = 0;
       bool ok = true;
       while (ok && it.valid) {
         const UnitInfo ui = it.ui;
         const int sb = g & 1;
-        if (!wait(&bar[B_P_FULL + sb], (g >> 1) & 1)) { ok = false; break; }
+        if (!wait_lazy(&bar[B_P_FULL + sb], (g >> 1) & 1)) { ok = false; break; }
         const uint8_t* msg = sPr + sb * L::kMsgStride;
         const uint32_t hdr = *reinterpret_cast<const volatile uint32_t*>(msg + L::kMsgHdr);
         const float alpha = reinterpret_cast<const float*>(msg + L::kMsgAlpha)[r];
         const float lsum = reinterpret_cast<const float*>(msg + L::kMsgL)[r];
+        const float m2 = reinterpret_cast<const float*>(msg + L::kMsgM)[r];
+        // the message's header fields are in registers: the slot may go back
+        // (once the PV MMAs have read its P as well)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[B_META_READ + sb]);
         if (hdr & 1u) {
           // O *= alpha before PV of this tile; PV of the previous tile must be done
-          if (!wait(&bar[B_PV_DONE + ((g - 1) & 1)], ((g - 1) >> 1) & 1)) { ok = false; break; }
+          if (!wait_lazy(&bar[B_PV_DONE + ((g - 1) & 1)], ((g - 1) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           for (int c0 = 0; c0 < 512; c0 += 32) {
             uint32_t v[32];
@@ -754,24 +855,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           if (lane == 0) mbar_arrive(&bar[B_O_FIXED]);
         }
         if (hdr & 2u) {
-          // epilogue: O / l -> o_part
-          if (!wait(&bar[B_PV_DONE + sb], (g >> 1) & 1)) { ok = false; break; }
+          // epilogue of the piece: O / l and its LSE
+          if (!wait_lazy(&bar[B_PV_DONE + sb], (g >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
+          const float lse2 = m2 + __log2f(lsum);          // log2 domain
           const int64_t row_out =
               (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H + r;
           const float inv_l = 1.f / lsum;
-          for (int c0 = 0; c0 < 512; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + c0, v);
-            tmem_wait_ld();
-            if (r < pp.H) store_row32(pp.o_part, row_out * 512 + c0, v, inv_l, pp.part_dtype);
+          if (it.whole()) {
+            for (int c0 = 0; c0 < 512; c0 += 32) {
+              uint32_t v[32];
+              tmem_ld32(tmem + lane_base + c0, v);
+              tmem_wait_ld();
+              if (r < pp.H) store_row32(pp.o_part, row_out * 512 + c0, v, inv_l, pp.part_dtype);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_O_EMPTY]);
+            if (r < pp.H) pp.lse_part[row_out] = lse2 * kLn2;
+          } else {
+            // a piece of a unit split across pairs: park O / l (in the
+            // partial dtype) and the LSE in this pair's workspace slot; the
+            // pieces are merged after the main loop
+            const int slot = 2 * cid + (it.u == rng.u_begin ? 0 : 1);
+            for (int c0 = 0; c0 < 512; c0 += 32) {
+              uint32_t v[32];
+              tmem_ld32(tmem + lane_base + c0, v);
+              tmem_wait_ld();
+              store_row32(pp.ws_o, (static_cast<int64_t>(slot) * 128 + r) * 512 + c0, v, inv_l,
+                          pp.part_dtype);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_O_EMPTY]);
+            pp.ws_lse[slot * 128 + r] = lse2;
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar[B_O_EMPTY]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[B_META_READ + sb]);
         it.advance(pp);
         ++g;
       }
@@ -780,6 +899,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (pp.split && rank == 1 && threadIdx.x == 0) {
+    // Record the split unit whose last tile this pair holds (if any) for the
+    // merge kernel: the unit at the start of the share, cut before it and
+    // ending inside it.  Written on every call with a workspace.
+    int4 rec = make_int4(-1, 0, 0, 0);
+    if (split && rng.u_begin <= rng.u_last && rng.j_begin > 0) {
+      const int nt = unit_info<TILE>(pp, rng.u_begin).ntiles;
+      if (rng.u_begin < rng.u_last || rng.j_stop == nt) {
+        const int64_t ustart = share_start(cid) - rng.j_begin;
+        rec = make_int4(rng.u_begin, static_cast<int>(ustart), cluster_of(ustart), cid);
+      }
+    }
+    pp.ws_units[cid] = rec;
+    if (cid == 0) pp.ws_units[ncl] = make_int4(static_cast<int>(share_total), ncl, 0, 0);
+  }
   cluster_sync();   // no DSMEM traffic into either CTA after this point
   if (warp == 1) {
     __syncwarp();
@@ -787,16 +921,115 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   }
 }
 
+// ---------------------------------------------------------------- merge of split units
+// One CTA per (pair, 64-row half): merges the pieces of the split unit whose
+// last tile that pair held (pp.ws_units[pair]) by their LSEs, exactly as the
+// combine merges shards, and writes the unit's o_part rows and lse_part.
+__global__ void __launch_bounds__(256) mla_partial_merge_kernel(PartialParams pp) {
+  griddep_wait();   // the partial grid has completed and its writes are visible
+  const int4 rec = pp.ws_units[blockIdx.x];
+  const int u = rec.x;
+  if (u < 0) return;
+  const int4 hdr = pp.ws_units[gridDim.x];
+  const int64_t total = hdr.x;
+  const int ncl = hdr.y;
+  const int64_t ustart = rec.y;
+  const int c_first = rec.z, c_last = rec.w;
+  auto share_start = [&](int c) -> int64_t { return static_cast<int64_t>(c) * total / ncl; };
+  __shared__ int s_slot[256];
+  __shared__ float s_w[256 * 32];       // per candidate pair, per row of the pass: weight
+  __shared__ float s_lsetot[32];
+  const int ncand = c_last - c_first + 1;
+  for (int i = threadIdx.x; i < ncand; i += 256) {
+    const int c = c_first + i;
+    s_slot[i] = share_start(c + 1) > share_start(c) ? 2 * c + (share_start(c) >= ustart ? 0 : 1) : -1;
+  }
+  const int sub = threadIdx.x & 7;      // 64-column slice of a row
+  const bool f32 = pp.part_dtype == kFP32;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int rbase = blockIdx.y * 64 + pass * 32;
+    __syncthreads();
+    for (int x = threadIdx.x; x < ncand * 32; x += 256) {
+      const int i = x >> 5, rr = x & 31;
+      const int sl = s_slot[i];
+      s_w[x] = (sl >= 0 && rbase + rr < pp.H) ? pp.ws_lse[sl * 128 + rbase + rr] : -INFINITY;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int rr = threadIdx.x;
+      float mx = -INFINITY;
+      for (int i = 0; i < ncand; ++i) mx = fmaxf(mx, s_w[i * 32 + rr]);
+      float wsum = 0.f;
+      for (int i = 0; i < ncand; ++i) wsum += s_slot[i] >= 0 ? exp2f(s_w[i * 32 + rr] - mx) : 0.f;
+      const float inv_w = 1.f / wsum;
+      for (int i = 0; i < ncand; ++i)
+        s_w[i * 32 + rr] = s_slot[i] >= 0 ? exp2f(s_w[i * 32 + rr] - mx) * inv_w : 0.f;
+      s_lsetot[rr] = (mx + __log2f(wsum)) * kLn2;
+    }
+    __syncthreads();
+    const int rr = threadIdx.x >> 3;
+    const int r = rbase + rr;
+    if (r >= pp.H) continue;
+    float acc[64];
+#pragma unroll
+    for (int t = 0; t < 64; ++t) acc[t] = 0.f;
+    for (int i = 0; i < ncand; ++i) {
+      const int sl = s_slot[i];
+      if (sl < 0) continue;
+      const float w = s_w[i * 32 + rr];
+      const int64_t e0 = (static_cast<int64_t>(sl) * 128 + r) * 512 + sub * 64;
+      if (f32) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(pp.ws_o) + e0);
+        float4 f[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) f[q] = src[q];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          acc[4 * q] = fmaf(w, f[q].x, acc[4 * q]);
+          acc[4 * q + 1] = fmaf(w, f[q].y, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(w, f[q].z, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(w, f[q].w, acc[4 * q + 3]);
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(pp.ws_o) + e0);
+        uint4 h[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) h[q] = src[q];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t hw[4] = {h[q].x, h[q].y, h[q].z, h[q].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f2 = unpack2(hw[j], pp.part_dtype);
+            acc[8 * q + 2 * j] = fmaf(w, f2.x, acc[8 * q + 2 * j]);
+            acc[8 * q + 2 * j + 1] = fmaf(w, f2.y, acc[8 * q + 2 * j + 1]);
+          }
+        }
+      }
+    }
+    const int64_t row = static_cast<int64_t>(u) * pp.H + r;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v[32];
+#pragma unroll
+      for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(acc[32 * h + t]);
+      store_row32(pp.o_part, row * 512 + sub * 64 + 32 * h, v, 1.f, pp.part_dtype);
+    }
+    if (sub == 0) pp.lse_part[row] = s_lsetot[rr];
+  }
+}
+
 // ---------------------------------------------------------------- launcher
+// Sets the kernel's shared-memory limit and finds how many CTA pairs fit on
+// the current device at once (cached per device).
 template <bool BF16>
-static int launch_partial_t(const CUtensorMap& qpe, const CUtensorMap& kv, const CUtensorMap& cur,
-                            const CUtensorMap& kv_v, const CUtensorMap& cur_v,
-                            const uint16_t* q_abs, const PartialParams& pp, cudaStream_t stream) {
-  auto kern = mla_partial_kernel<BF16>;
-  constexpr int smem = PairSmem::kTotal;
-  static bool configured = false;
-  static int max_clusters = 0;
-  if (!configured) {
+static int prepare_partial(int* clusters) {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  if (cache[dev] == 0) {
+    auto kern = mla_partial_kernel<BF16>;
+    constexpr int smem = PairSmem::kTotal;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return -1;
@@ -811,15 +1044,46 @@ static int launch_partial_t(const CUtensorMap& qpe, const CUtensorMap& kv, const
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess ||
-        max_clusters < 1) {
-      cudaGetLastError();
-      max_clusters = 64;
-    }
-    configured = true;
+    int mc = 0;
+    if (cudaOccupancyMaxActiveClusters(&mc, kern, &cfg) != cudaSuccess || mc < 1) return -1;
+    cache[dev] = std::min(mc, 256);   // the partition keeps per-pair state in 256-entry arrays
   }
-  const int clusters = std::max(1, std::min(pp.num_units, max_clusters));
-  kern<<<dim3(2 * clusters), dim3(256), smem, stream>>>(qpe, kv, cur, kv_v, cur_v, q_abs, pp);
+  *clusters = cache[dev];
+  return 0;
+}
+
+int partial_max_clusters() {
+  int a = 0, b = 0;
+  if (prepare_partial<true>(&a) != 0 || prepare_partial<false>(&b) != 0) return -1;
+  return std::min(a, b);
+}
+
+template <bool BF16>
+static int launch_partial_t(const CUtensorMap& qpe, const CUtensorMap& kv, const CUtensorMap& cur,
+                            const CUtensorMap& kv_v, const CUtensorMap& cur_v,
+                            const uint16_t* q_abs, const PartialParams& pp, cudaStream_t stream) {
+  int max_clusters = 0;
+  if (prepare_partial<BF16>(&max_clusters) != 0) return -1;
+  // with a workspace every resident pair takes an equal share of the tiles
+  const int clusters = pp.split ? pp.split : std::max(1, std::min(pp.num_units, max_clusters));
+  if (clusters > max_clusters) return -1;
+  mla_partial_kernel<BF16><<<dim3(2 * clusters), dim3(256), PairSmem::kTotal, stream>>>(
+      qpe, kv, cur, kv_v, cur_v, q_abs, pp);
+  if (pp.split) {
+    // programmatic dependent launch: the merge grid is scheduled while the
+    // partial grid drains and waits for it on the device (griddepcontrol)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(clusters, 2, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, mla_partial_merge_kernel, pp) != cudaSuccess) return -1;
+  }
   return 0;
 }
 

@@ -15,6 +15,9 @@ namespace mla {
 // 2^22 polls (tens of ms to a few seconds): far beyond any legitimate wait
 // in these kernels, short enough that a fault unwinds quickly.
 constexpr uint32_t kSpinLimit = 1u << 22;
+// Suspend hint of the lazy waits (ns); with it a wait ends after at most
+// kSpinLimit polls of up to this long each.
+constexpr uint32_t kLazyWaitNs = 1000;
 
 // Error codes written to the device error word (first writer wins).
 enum DeviceError : int {
@@ -83,6 +86,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended for up to `ns`
+// nanoseconds (it resumes as soon as the phase completes): for waits of many
+// threads that are off the critical path, so their polling does not compete
+// with the issuing threads for the shared-memory pipeline.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred P;\n mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, P;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -139,6 +157,16 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
                "f"(c), "f"(d)
                : "memory");
+}
+
+
+// Programmatic dependent launch: let the next grid on the stream be
+// scheduled early / wait until the previous grid has completed.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {

@@ -48,13 +48,13 @@ ODD = ctypes.c_void_p(0x10008)       # 8-byte aligned only
 def _partial(lib, **over):
     args = dict(q_abs=FAKE, q_pe=FAKE, kv=FAKE, table=FAKE, lens=FAKE, cur=None, B=2, q=1,
                 H=128, nb=10, bs=32, mb=5, S=2, scale=0.07, idt=0, pdt=0, o=FAKE, l=FAKE,
-                err=None)
+                err=None, ws=None, wsb=0)
     args.update(over)
     a = args
     return lib.mla_dcp_decode_partial(a["q_abs"], a["q_pe"], a["kv"], a["table"], a["lens"],
                                       a["cur"], a["B"], a["q"], a["H"], a["nb"], a["bs"],
                                       a["mb"], a["S"], a["scale"], a["idt"], a["pdt"], a["o"],
-                                      a["l"], a["err"], None)
+                                      a["l"], a["err"], a["ws"], a["wsb"], None)
 
 
 def test_partial_host_checks(lib):
@@ -68,6 +68,13 @@ def test_partial_host_checks(lib):
     assert _partial(lib, S=65) == 5
     assert _partial(lib, bs=48) == 6
     assert _partial(lib, kv=ODD) == 4
+    assert _partial(lib, ws=ctypes.c_void_p(0x10010), wsb=1 << 20) == 4   # workspace not 256-aligned
+
+
+def test_workspace_size_rejects_bad_sizes(lib):
+    assert lib.mla_dcp_decode_partial_workspace_size(0, 1, 2, 0) == 0
+    assert lib.mla_dcp_decode_partial_workspace_size(2, 9, 2, 0) == 0
+    assert lib.mla_dcp_decode_partial_workspace_size(2, 1, 65, 1) == 0
 
 
 def test_combine_vup_gather_host_checks(lib):

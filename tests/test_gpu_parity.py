@@ -195,6 +195,45 @@ def test_equal_logit_rows():
     assert_out_close(f64(out), ref_out, "out")
 
 
+# ------------------------------------------------------------------ work split across CTA pairs
+@pytest.mark.parametrize("name", ["ragged_bf16_cur", "mtp_fp16", "heads16_fp32part"])
+def test_whole_shards_without_workspace(name):
+    """Without a workspace every CTA pair takes whole shards; same results."""
+    dp = DeviceProblem(inputs.make_problem(SMALL[name]))
+    o_part, lse_part = dp.partial(workspace=None)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    _check_partials(dp, o_part, lse_part)
+
+
+@pytest.mark.parametrize("history,q_len,cur", [(40000, 1, False), (9000, 2, True),
+                                                  (3000, 1, False)])
+def test_shard_split_over_many_pairs(history, q_len, cur):
+    """Few long shards cut into pieces of a few tiles for every CTA pair (with
+    3000 tokens there are fewer tiles than pairs, so pairs with empty shares
+    sit between the pieces): the merged pieces must equal the oracle, and a
+    second call on the same (uninitialised) workspace gives identical results."""
+    cfg = inputs.DecodeConfig(name="sp", batch=1, heads=128, q_len=q_len, num_shards=1,
+                              block_size=64, history=history, current=cur, seed=101)
+    dp = DeviceProblem(inputs.make_problem(cfg))
+    nbytes = api._ffi.lib().mla_dcp_decode_partial_workspace_size(1, q_len, 1, int(cur))
+    ws = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device=dp.dev)
+    o1, l1 = dp.partial(workspace=ws, part_dtype=torch.float32)
+    o2, l2 = dp.partial(workspace=ws, part_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    _check_partials(dp, o1, l1)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_workspace_too_small_is_rejected():
+    dp = DeviceProblem(inputs.make_problem(SMALL["tiny"]))
+    ws = torch.zeros(1024, dtype=torch.uint8, device=dp.dev)
+    with pytest.raises(api._ffi.MlaError) as e:
+        dp.partial(workspace=ws)
+    assert e.value.status == 2
+
+
 # ------------------------------------------------------------------ streams and errors
 def test_user_stream_no_implicit_sync():
     dp = DeviceProblem(inputs.make_problem(SMALL["ragged_bf16_cur"]))
