@@ -337,7 +337,7 @@ def run_ours(args, rank, world, local_rank):
         roof = {"bound": "tensor", "achieved": round(tc_ach, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(tc_frac, 4)}
     roof["traffic"] = traffic_from_profile(args.config)
-    roof["kernel"] = "mla_partial_kernel"
+    roof["kernel"] = "mla_partial_kernel (+ mla_partial_merge_kernel)"
     roof["kernel_ms"] = round(partial_ms, 5)
     roof["alg_bytes_per_launch"] = wm["partial_bytes"]
     roof["alg_flops_per_launch"] = wm["partial_flops"]
@@ -372,7 +372,8 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roof,
         "e2e": {"value": round(e2e_tbs, 4), "unit": "TB/s",
                 "h2d_bytes_per_step": wm["h2d_bytes"], "d2h_bytes_per_step": wm["d2h_bytes"]},
-        "gpu_launches": 2 * args.steps,
+        # per step: partial kernel, its split-shard merge kernel, fused combine + V-up
+        "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
