@@ -141,6 +141,34 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
 uint64_t mla_dcp_decode_partial_workspace_size(int B, int q_len, int num_shards, int has_current);
 
 /*
+ * mla_dcp_decode_partial_noalloc -- mla_dcp_decode_partial with no
+ * workspace argument and no allocation of any kind.  A library addition
+ * with no counterpart in the sources.
+ *
+ * Same arguments, results and errors as mla_dcp_decode_partial, whose
+ * split-shard workspace it takes from a fixed 24 MiB device array inside the
+ * library.  That holds the workspace of up to 95 CTA pairs with BF16 / FP16
+ * partials, or 47 with FP32 partials; when this device needs more (e.g. FP32
+ * partials on a GPU with more than 47 resident pairs) the call returns
+ * MLA_ERR_BAD_SHAPE and launches nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) and the kernel's occupancy; make that first call
+ *     outside any stream capture.  Later calls only launch kernels, so they
+ *     can be captured into a CUDA graph.
+ *   - Nothing in the array has to start at zero: every call rewrites each
+ *     record it reads.
+ *   - All calls on a device share the array: calls that may overlap in time
+ *     (different streams, or graphs replayed concurrently) race on it and
+ *     must be serialised by the caller.
+ */
+int mla_dcp_decode_partial_noalloc(const void* q_abs, const void* q_pe, const void* kv_cache,
+                                   const int32_t* block_table, const int32_t* seq_lens,
+                                   const void* kv_cur, int B, int q_len, int H, int num_blocks,
+                                   int block_size, int max_blocks, int num_shards, float scale,
+                                   int in_dtype, int part_dtype, void* o_part, float* lse_part,
+                                   int32_t* err_flag, mla_stream_t stream);
+
+/*
  * mla_lse_combine -- merge partials by their log-sum-exps.
  *
  * Defines: [PR] glossary "LSE" and the fourth change (combine without packing the

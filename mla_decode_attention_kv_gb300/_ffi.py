@@ -23,6 +23,8 @@ SIGNATURES = {
     "mla_dcp_decode_partial": (I, [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, P, P, P,
                                    ctypes.c_uint64, P]),
     "mla_dcp_decode_partial_workspace_size": (ctypes.c_uint64, [I, I, I, I]),
+    "mla_dcp_decode_partial_noalloc": (I, [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, P, P,
+                                           P]),
     "mla_lse_combine": (I, [P, P, I, P, P, I, I, I, I, P, P, P]),
     "mla_vup": (I, [P, P, I, I, I, P, P, P]),
     "mla_lse_combine_vup": (I, [P, P, I, P, P, P, I, I, I, I, P, P, P, P, P]),

@@ -102,6 +102,27 @@ def mla_dcp_decode_partial(q_abs, q_pe, kv_cache, block_table, seq_lens, num_sha
     return o_part, lse_part
 
 
+def mla_dcp_decode_partial_noalloc(q_abs, q_pe, kv_cache, block_table, seq_lens,
+                                   num_shards: int, *, o_part, lse_part, kv_cur=None,
+                                   scale: float = DEFAULT_SCALE, err_flag=None, stream=None):
+    """mla_dcp_decode_partial with the library's fixed scratch array instead of
+    a workspace: allocates nothing (o_part / lse_part are required).  Calls
+    that may overlap in time share that array and must be serialised."""
+    B, q_len, H, _ = q_abs.shape
+    num_blocks, bs, _ = kv_cache.shape
+    for t, n in ((q_abs, "q_abs"), (q_pe, "q_pe"), (kv_cache, "kv_cache"),
+                 (block_table, "block_table"), (seq_lens, "seq_lens"), (o_part, "o_part"),
+                 (lse_part, "lse_part")):
+        _need(t, n)
+    st = _ffi.lib().mla_dcp_decode_partial_noalloc(
+        _p(q_abs), _p(q_pe), _p(kv_cache), _p(block_table), _p(seq_lens), _p(kv_cur),
+        B, q_len, H, num_blocks, bs, block_table.shape[1], num_shards, float(scale),
+        _code(q_abs.dtype), _code(o_part.dtype), _p(o_part), _p(lse_part), _p(err_flag),
+        _s(stream))
+    _ffi.check("mla_dcp_decode_partial_noalloc", st)
+    return o_part, lse_part
+
+
 def _rows(o_part, lse_part):
     """View [..., P, H, 512] partials as T rows."""
     P, H = o_part.shape[-3], o_part.shape[-2]

@@ -157,7 +157,8 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
   if (workspace) {
     const int clusters = mla::partial_max_clusters();
     if (clusters < 1) return MLA_ERR_CUDA;
-    if (workspace_bytes < mla::partial_workspace_bytes(clusters)) return MLA_ERR_BAD_SHAPE;
+    const int part_bytes = part_dtype == MLA_FP32 ? 4 : 2;
+    if (workspace_bytes < mla::partial_workspace_bytes(clusters, part_bytes)) return MLA_ERR_BAD_SHAPE;
     const size_t recs = (static_cast<size_t>(clusters + 1) * 16 + 255) / 256 * 256;
     char* w = static_cast<char*>(workspace);
     pp.split = clusters;
@@ -176,6 +177,47 @@ uint64_t mla_dcp_decode_partial_workspace_size(int B, int q_len, int num_shards,
   const int clusters = mla::partial_max_clusters();
   if (clusters < 1) return 0;
   return mla::partial_workspace_bytes(clusters);
+}
+
+// ------------------------------------------------------------------ no-alloc variant
+// Scratch of mla_dcp_decode_partial_noalloc: a fixed device array, so the
+// call needs no allocation of any kind.  24 MiB holds the split-shard
+// workspace of up to 95 CTA pairs with 16-bit partials (47 with fp32).
+constexpr size_t kNoAllocScratchBytes = size_t{24} << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+// Device address of g_noalloc_scratch, looked up once per device.
+void* noalloc_scratch() {
+  static void* addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev] && cudaGetSymbolAddress(&addr[dev], g_noalloc_scratch) != cudaSuccess) {
+    cudaGetLastError();
+    addr[dev] = nullptr;
+  }
+  return addr[dev];
+}
+}  // namespace
+
+int mla_dcp_decode_partial_noalloc(const void* q_abs, const void* q_pe, const void* kv_cache,
+                                   const int32_t* block_table, const int32_t* seq_lens,
+                                   const void* kv_cur, int B, int q_len, int H, int num_blocks,
+                                   int block_size, int max_blocks, int num_shards, float scale,
+                                   int in_dtype, int part_dtype, void* o_part, float* lse_part,
+                                   int32_t* err_flag, mla_stream_t stream) {
+  if (!is_part_dtype(part_dtype)) return MLA_ERR_BAD_DTYPE;
+  const int clusters = mla::partial_max_clusters();
+  if (clusters < 1) return MLA_ERR_CUDA;
+  const size_t need = mla::partial_workspace_bytes(clusters, part_dtype == MLA_FP32 ? 4 : 2);
+  if (need > kNoAllocScratchBytes) return MLA_ERR_BAD_SHAPE;
+  void* scratch = noalloc_scratch();
+  if (!scratch) return MLA_ERR_CUDA;
+  return mla_dcp_decode_partial(q_abs, q_pe, kv_cache, block_table, seq_lens, kv_cur, B, q_len, H,
+                                num_blocks, block_size, max_blocks, num_shards, scale, in_dtype,
+                                part_dtype, o_part, lse_part, err_flag, scratch, need, stream);
 }
 
 int mla_lse_combine(const void* o_part, const float* lse_part, int num_parts, const void* o_local,

@@ -29,11 +29,12 @@ struct PartialParams {
   int4* ws_units;        // [pairs + 1]: {unit, first tile, first pair, last pair}; header {T, pairs}
 };
 
-// Workspace of the partial kernel for `clusters` CTA pairs.
-inline size_t partial_workspace_bytes(int clusters) {
+// Workspace of the partial kernel for `clusters` CTA pairs and partials of
+// `part_bytes` bytes per element (4 covers every partial dtype).
+inline size_t partial_workspace_bytes(int clusters, int part_bytes = 4) {
   const size_t slots = 2 * static_cast<size_t>(clusters);
   const size_t recs = (static_cast<size_t>(clusters + 1) * 16 + 255) / 256 * 256;
-  return recs + slots * 128 * 4 + slots * 512 * 128 * 4;
+  return recs + slots * 128 * 4 + slots * 512 * 128 * static_cast<size_t>(part_bytes);
 }
 int partial_max_clusters();
 
