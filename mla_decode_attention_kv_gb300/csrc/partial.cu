@@ -181,12 +181,29 @@ static_assert(PairSmem::kPrOff + 2 * PairSmem::kMsgStride <= PairSmem::kBarOff, 
 static_assert(PairSmem::kTotal <= 232448, "shared memory budget");
 
 // Barrier slots in the common block.
+// (derived from the ring sizes, so a deeper ring cannot make slots overlap)
 enum : int {
-  B_KFULL = 0, B_KEMPTY = 10, B_QR_FULL = 20, B_Q_EMPTY = 21, B_QLAT_FULL = 22, B_S_FULL = 23,
-  B_S_EMPTY = 25, B_PFREE = 27, B_MMA_DONE_A = 29,
-  B_VFULL = 30, B_VEMPTY = 34, B_P_FULL = 38, B_PV_DONE = 40, B_META_READ = 42, B_O_EMPTY = 44,
-  B_O_FIXED = 45, B_MMA_DONE_B = 46, B_COUNT = 47
+  B_KFULL = 0,
+  B_KEMPTY = B_KFULL + PairSmem::kNK,
+  B_QR_FULL = B_KEMPTY + PairSmem::kNK,
+  B_Q_EMPTY = B_QR_FULL + 1,
+  B_QLAT_FULL = B_Q_EMPTY + 1,
+  B_S_FULL = B_QLAT_FULL + 1,      // 2
+  B_S_EMPTY = B_S_FULL + 2,        // 2
+  B_PFREE = B_S_EMPTY + 2,         // 2
+  B_MMA_DONE_A = B_PFREE + 2,
+  B_VFULL = B_MMA_DONE_A + 1,
+  B_VEMPTY = B_VFULL + PairSmem::kNV,
+  B_P_FULL = B_VEMPTY + PairSmem::kNV,   // 2
+  B_PV_DONE = B_P_FULL + 2,        // 2
+  B_META_READ = B_PV_DONE + 2,     // 2
+  B_O_EMPTY = B_META_READ + 2,
+  B_O_FIXED = B_O_EMPTY + 1,
+  B_MMA_DONE_B = B_O_FIXED + 1,
+  B_COUNT = B_MMA_DONE_B + 1
 };
+// barriers + TMEM slot + abort flag + 4 warp flags must fit the barrier block
+static_assert((B_COUNT + 1) * 8 + 8 + 16 <= 512, "barrier block");
 
 template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
