@@ -237,6 +237,9 @@ __global__ void __launch_bounds__(256, 1)
       for (int kh = 0; kh < 2; ++kh)
         tma_load_2d(sW + g * 65536 + kh * 32768, &tm_w, &bar_w, g * 64, h * 512 + kh * 256, pol);
   }
+  // W_UV does not depend on the previous kernel; the partials do (programmatic
+  // dependent launch: wait here for the grid that wrote them)
+  griddep_wait();
   constexpr uint32_t idesc = make_idesc_f16(128, kVupRows, BF16, true, false);
   bool ok = true;
   int phase = 0;
@@ -246,7 +249,8 @@ __global__ void __launch_bounds__(256, 1)
     const int c = lane >> 2;          // 64-element chunk of this lane's 16 values
     const int u = 2 * (lane & 3);     // first 16-byte unit inside the 128-byte row
     if constexpr (COMBINE) {
-      for (int rr = warp * 2; rr < kVupRows; rr += 16) {
+      // rows past nrows are left unwritten: their D columns are never stored
+      for (int rr = warp * 2; rr < nrows; rr += 16) {
         const int64_t t[2] = {t0 + rr, t0 + rr + 1};
         const bool valid[2] = {rr < nrows, rr + 1 < nrows};
         float acc[2][16];
@@ -272,9 +276,9 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
     } else {
-      for (int rr = warp; rr < kVupRows; rr += 8) {
+      for (int rr = warp; rr < nrows; rr += 8) {
         uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-        if (rr < nrows) {
+        {
           const uint4* src = reinterpret_cast<const uint4*>(
               static_cast<const uint16_t*>(o_latent_in) +
               ((t0 + rr) * static_cast<int64_t>(H) + h) * 512 + lane * 16);
@@ -369,8 +373,19 @@ static int launch_vup_t(const CUtensorMap& tm_w, const void* o_part, const float
       return -1;
     configured = true;
   }
-  kern<<<H, 256, kVupSmem, stream>>>(tm_w, o_part, lse_part, P, o_local, lse_local, o_latent_in,
-                                     T, H, part_dt, out, o_latent_out, lse_out, err);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(H, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = kVupSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, tm_w, o_part, lse_part, P, o_local, lse_local, o_latent_in, T,
+                         H, part_dt, out, o_latent_out, lse_out, err) != cudaSuccess)
+    return -1;
   return 0;
 }
 

@@ -944,6 +944,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 // combine merges shards, and writes the unit's o_part rows and lse_part.
 __global__ void __launch_bounds__(256) mla_partial_merge_kernel(PartialParams pp) {
   griddep_wait();   // the partial grid has completed and its writes are visible
+  griddep_launch_dependents();
   const int4 rec = pp.ws_units[blockIdx.x];
   const int u = rec.x;
   if (u < 0) return;
