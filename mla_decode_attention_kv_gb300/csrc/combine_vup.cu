@@ -366,12 +366,15 @@ static int launch_vup_t(const CUtensorMap& tm_w, const void* o_part, const float
                         int T, int H, int part_dt, void* out, void* o_latent_out, float* lse_out,
                         int* err, cudaStream_t stream) {
   auto kern = mla_vup_kernel<COMBINE, BF16, F32>;
-  static bool configured = false;
-  if (!configured) {
+  // the shared-memory limit is a per-device function attribute
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  if (!configured[dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kVupSmem) !=
         cudaSuccess)
       return -1;
-    configured = true;
+    configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(H, 1, 1);
