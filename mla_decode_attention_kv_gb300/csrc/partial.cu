@@ -294,7 +294,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   // pair compute the same range.
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(nclusters_x());
-  __shared__ int s_scan[256];
+  __shared__ int s_scan[8];
   __shared__ int s_load[256];
   __shared__ int s_rng[8];
   TileRange rng;
@@ -316,7 +316,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     const int e = min(U, a + per);
     int cnt = 0;
     for (int u = a; u < e; ++u) cnt += unit_info<TILE>(pp, u).ntiles;
-    s_scan[threadIdx.x] = cnt;
+    // exclusive block scan of cnt: warp inclusive scans, then the warp totals
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_scan[warp] = incl;   // warp totals (s_scan reused below)
     if (threadIdx.x == 0) {
       s_rng[0] = INT_MAX;   // u_begin
       s_rng[1] = 0;         // j_begin
@@ -324,44 +331,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       s_rng[3] = 0;         // j_stop
       s_rng[4] = U;         // ue0
       s_rng[5] = U;         // ue1
-      s_rng[7] = 0;         // split
     }
     for (int c = threadIdx.x; c < ncl; c += 256) s_load[c] = 0;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int run = 0;
-      for (int i = 0; i < 256; ++i) {
-        const int c = s_scan[i];
-        s_scan[i] = run;
-        run += c;
-      }
-      s_rng[6] = run;
+    int warp_base = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int t = s_scan[w];
+      warp_base += w < warp ? t : 0;
+      all += t;
     }
-    __syncthreads();
-    share_total = s_rng[6];
+    const int my_start = warp_base + incl - cnt;   // tiles before this thread's units
+    share_total = all;
     if (pp.split && share_total > 0) {
       // Split units only where whole units would leave the busiest pair above
       // the even share by more than max(2 tiles, 1/8 of the share): the
       // merge kernel and the extra unit ends cost about that much.
-      int64_t run = s_scan[threadIdx.x];
+      int64_t run = my_start;
       for (int u = a; u < e; ++u) {
         const int nt = unit_info<TILE>(pp, u).ntiles;
         if (nt > 0) atomicAdd(&s_load[cluster_of(run)], nt);
         run += nt;
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        int mx = 0;
-        for (int c = 0; c < ncl; ++c) mx = max(mx, s_load[c]);
-        const int64_t even = (share_total + ncl - 1) / ncl;
-        s_rng[7] = mx > even + max(int64_t{2}, even / 8) ? 1 : 0;
-      }
-      __syncthreads();
-      split = s_rng[7] != 0;
+      int mx = 0;
+      for (int c = threadIdx.x; c < ncl; c += 256) mx = max(mx, s_load[c]);
+      const int64_t even = (share_total + ncl - 1) / ncl;
+      // any pair above the threshold decides for all
+      split = __syncthreads_or(mx > even + max(int64_t{2}, even / 8)) != 0;
     }
     const int64_t lo = share_start(cid);
     const int64_t hi = share_start(cid + 1);
-    int64_t run = s_scan[threadIdx.x];
+    int64_t run = my_start;
     for (int u = a; u < e; ++u) {
       const int nt = unit_info<TILE>(pp, u).ntiles;
       if (run >= lo) atomicMin(&s_rng[4], u);
@@ -880,11 +881,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
               (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H + r;
           const float inv_l = 1.f / lsum;
           if (it.whole()) {
-            for (int c0 = 0; c0 < 512; c0 += 32) {
-              uint32_t v[32];
-              tmem_ld32(tmem + lane_base + c0, v);
+            // two TMEM loads in flight per wait
+            for (int c0 = 0; c0 < 512; c0 += 64) {
+              uint32_t v0[32], v1[32];
+              tmem_ld32(tmem + lane_base + c0, v0);
+              tmem_ld32(tmem + lane_base + c0 + 32, v1);
               tmem_wait_ld();
-              if (r < pp.H) store_row32(pp.o_part, row_out * 512 + c0, v, inv_l, pp.part_dtype);
+              if (r < pp.H) {
+                store_row32(pp.o_part, row_out * 512 + c0, v0, inv_l, pp.part_dtype);
+                store_row32(pp.o_part, row_out * 512 + c0 + 32, v1, inv_l, pp.part_dtype);
+              }
             }
             tc_fence_before();
             __syncwarp();
@@ -895,12 +901,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             // partial dtype) and the LSE in this pair's workspace slot; the
             // pieces are merged after the main loop
             const int slot = 2 * cid + (it.u == rng.u_begin ? 0 : 1);
-            for (int c0 = 0; c0 < 512; c0 += 32) {
-              uint32_t v[32];
-              tmem_ld32(tmem + lane_base + c0, v);
+            for (int c0 = 0; c0 < 512; c0 += 64) {
+              uint32_t v0[32], v1[32];
+              tmem_ld32(tmem + lane_base + c0, v0);
+              tmem_ld32(tmem + lane_base + c0 + 32, v1);
               tmem_wait_ld();
-              store_row32(pp.ws_o, (static_cast<int64_t>(slot) * 128 + r) * 512 + c0, v, inv_l,
-                          pp.part_dtype);
+              const int64_t e = (static_cast<int64_t>(slot) * 128 + r) * 512 + c0;
+              store_row32(pp.ws_o, e, v0, inv_l, pp.part_dtype);
+              store_row32(pp.ws_o, e + 32, v1, inv_l, pp.part_dtype);
             }
             tc_fence_before();
             __syncwarp();
