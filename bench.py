@@ -403,7 +403,37 @@ def cpu_baseline(prob, budget_s: float):
     return {"value": round(kv / dt / 1e12, 9), "unit": "TB/s", "cores": _CPU_THREADS,
             "kind": "oracle",
             "sample": f"{n} of {cfg.batch} sequences (all {cfg.heads} heads, full history) "
-                      f"in {dt:.1f} s, fp64 numpy oracle, {_CPU_THREADS} BLAS threads"}
+                      f"in {dt:.1f} s, fp64 numpy oracle, {_CPU_THREADS} BLAS threads",
+            "value_1thread": _cpu_one_thread(cfg.name, budget_s / 3)}
+
+
+def _cpu_one_thread(config: str, budget_s: float):
+    """The same oracle sample with BLAS limited to one thread (a child process,
+    since the thread count is fixed when numpy loads); None if it fails."""
+    env = dict(os.environ)
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = "1"
+    try:
+        res = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-probe", config,
+                              str(budget_s)], env=env, capture_output=True, text=True,
+                             timeout=max(60.0, 6 * budget_s))
+        return json.loads(res.stdout.strip().splitlines()[-1])["value"]
+    except Exception:
+        return None
+
+
+def _cpu_probe(config: str, budget_s: float):
+    """Child of _cpu_one_thread: time the oracle on whole sequences of `config`."""
+    prob = inputs.make_problem(inputs.CONFIGS[config])
+    t0 = time.perf_counter()
+    _oracle_sample(prob, [0])
+    one = time.perf_counter() - t0
+    n = int(max(1, min(prob.cfg.batch, budget_s / max(one, 1e-3))))
+    t0 = time.perf_counter()
+    _oracle_sample(prob, list(range(n)))
+    dt = time.perf_counter() - t0
+    kv = int(prob.seq_lens[:n].astype(np.int64).sum()) * inputs.D_QK * 2
+    print(json.dumps({"value": round(kv / dt / 1e12, 9)}))
 
 
 def run_reference(args, rank, world):
@@ -452,7 +482,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="budget of the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-probe", nargs=2, metavar=("CONFIG", "SECONDS"), help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_probe:
+        _cpu_probe(args.cpu_probe[0], float(args.cpu_probe[1]))
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank = int(os.environ.get("RANK", "0"))
