@@ -579,7 +579,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         if (it.first()) {
           if (it.newq) {
             // Q latent row r -> TMEM (packed pairs, low half = even element)
-            if (it.nq >= 1 && !wait_lazy(&bar[B_Q_EMPTY], (it.nq - 1) & 1)) { ok = false; break; }
+            // (the softmax warps meet at named barriers, so every exit
+            // decision is made together through named_bar_and)
+            const bool qe = it.nq < 1 || wait_lazy(&bar[B_Q_EMPTY], (it.nq - 1) & 1);
+            if (!named_bar_and(1, 128, qe)) { ok = false; break; }
             tc_fence_after();
             const uint4* src = reinterpret_cast<const uint4*>(
                 q_abs + (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.H + r) * 512);
@@ -612,7 +615,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           l = 0.f;
         }
         const int sb = g & 1;
-        if (!wait_lazy(&bar[B_S_FULL + sb], (g >> 1) & 1)) { ok = false; break; }
+        if (!named_bar_and(1, 128, wait_lazy(&bar[B_S_FULL + sb], (g >> 1) & 1))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         float s[TILE];
         {
@@ -697,7 +703,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             bulk_commit();
           }
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0) && !*abort_flag;
+        ok = named_bar_and(1, 128, ok && !*abort_flag);
         it.advance(pp);
         ++g;
       }

@@ -334,6 +334,20 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also ANDs a predicate over the participating threads:
+// every participant gets the same result, so a group can leave a loop
+// together (no participant is left waiting at a later barrier).
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n barrier.red.and.pred p, %2, %3, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // Swizzled byte offset of 16-byte unit `u` of row `r` inside a tile whose
 // rows are 128 bytes and whose 8-row atoms are 1024-byte aligned (the
 // SWIZZLE_128B pattern shared by TMA and UMMA).
