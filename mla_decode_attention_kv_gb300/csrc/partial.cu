@@ -621,21 +621,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         }
         tc_fence_after();
         float s[TILE];
+        // S in four 32-column loads, one at a time, each folded into the row
+        // max before the next is issued: register-bound TMEM reads slow the
+        // SM's TMA stream, and they do so least when they are not bursts
+        const int nvalid = min(TILE, ui.hi - (ui.lo + it.j * TILE));
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         {
-          // four loads in flight, one wait
-          uint32_t v0[32], v1[32], v2[32], v3[32];
           const uint32_t sa = tmem + lane_base + kSCol + sb * TILE;
-          tmem_ld32(sa, v0);
-          tmem_ld32(sa + 32, v1);
-          tmem_ld32(sa + 64, v2);
-          tmem_ld32(sa + 96, v3);
-          tmem_wait_ld();
 #pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            s[t] = __uint_as_float(v0[t]);
-            s[32 + t] = __uint_as_float(v1[t]);
-            s[64 + t] = __uint_as_float(v2[t]);
-            s[96 + t] = __uint_as_float(v3[t]);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld32(sa + 32 * c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+              const int tt = 32 * c + t;
+              s[tt] = tt < nvalid ? __uint_as_float(v[t]) * pp.scale_log2 : -INFINITY;
+              mx[t & 3] = fmaxf(mx[t & 3], s[tt]);
+            }
           }
         }
         tc_fence_before();
@@ -643,13 +646,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         if (lane == 0) mbar_arrive(&bar[B_S_EMPTY + sb]);
 
         // ---- online softmax in the log2 domain
-        const int nvalid = min(TILE, ui.hi - (ui.lo + it.j * TILE));
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int t = 0; t < TILE; ++t) {
-          s[t] = t < nvalid ? s[t] * pp.scale_log2 : -INFINITY;
-          mx[t & 3] = fmaxf(mx[t & 3], s[t]);
-        }
         const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         bool need_rescale = false;
         float alpha = 1.f;
