@@ -107,11 +107,18 @@ def load_peaks():
 
 
 def kernel_source_sha() -> str:
+    """Hash of the partial kernel's sources with comments and blank lines
+    removed, so that editing a comment does not disown the ncu counters."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_decode_attention_kv_gb300", "csrc")
     for name in ("partial.cu", "ptx.cuh", "common.cuh", "kernels.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 

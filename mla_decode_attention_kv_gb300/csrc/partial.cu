@@ -20,13 +20,20 @@
 //   rank 0 ("QK CTA"): Q's latent part lives in its TMEM (the A operand of
 //     tcgen05 MMAs straight from tensor memory), the RoPE part in SMEM;
 //     S = Q K^T for 128-token tiles (N = 128) into two TMEM buffers; online
-//     softmax; P (bf16/fp16) plus per-row rescale factors and final row sums
-//     are shipped to rank 1 with one shared-memory-to-shared-memory bulk copy
-//     per tile (DSMEM, 256 B per token, one direction).
+//     softmax; P (bf16/fp16) plus per-row rescale factor, row sum and running
+//     max are shipped to rank 1 with one shared-memory-to-shared-memory bulk
+//     copy per tile (DSMEM, 256 B per token, one direction).
 //   rank 1 ("PV CTA"): the full fp32 O [128 x 512] in its TMEM; O += P V with
-//     N = 256 MMAs; rescale of O when the running max moved; epilogue O / l.
+//     N = 256 MMAs; rescale of O when the running max moved; epilogue O / l
+//     and the LSE.
 // Each CTA TMA-loads the KV columns it needs (rank 0 all 576, rank 1 the 512
 // latent ones, close in time so the second read hits L2).
+//
+// Scheduling: a persistent grid of every co-resident pair.  The units' tiles
+// form one flat sequence that the pairs share either as whole units or, with
+// a workspace and when whole units would be uneven, as exact tile shares; a
+// unit cut between pairs leaves pieces (O / l and LSE) in the workspace that
+// mla_partial_merge_kernel combines afterwards.
 //
 // Warp roles (256 threads per CTA):
 //   rank 0: w0 TMA producer (K chunks + Q RoPE), w1 MMA issuer, w2-3 LSE of
