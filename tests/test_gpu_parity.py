@@ -195,6 +195,34 @@ def test_equal_logit_rows():
     assert_out_close(f64(out), ref_out, "out")
 
 
+# ------------------------------------------------------------------ page sizes and query counts
+@pytest.mark.parametrize("bs", [128, 256])
+def test_large_pages(bs):
+    """128- and 256-token pages: one TMA box per chunk on the QK CTA, and
+    partial tiles at the ends of shards that start inside a page."""
+    cfg = inputs.DecodeConfig(name=f"pg{bs}", batch=3, heads=128, q_len=1, num_shards=3,
+                              block_size=bs, ragged=(400, 3000), current=True, seed=111)
+    dp = DeviceProblem(inputs.make_problem(cfg))
+    o_part, lse_part = dp.partial()
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    _check_partials(dp, o_part, lse_part)
+
+
+def test_many_query_tokens_few_heads():
+    """q_len 4 with the causal CURRENT chunk and 64 heads (half-filled MMA rows)."""
+    cfg = inputs.DecodeConfig(name="q4", batch=2, heads=64, q_len=4, num_shards=2,
+                              block_size=64, ragged=(50, 700), current=True, seed=121)
+    dp = DeviceProblem(inputs.make_problem(cfg))
+    out = dp.step()
+    o_part, lse_part = dp.partial()
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    _check_partials(dp, o_part, lse_part)
+    _, _, ref_out = om.decode_reference(dp.prob)
+    assert_out_close(f64(out), ref_out, "out")
+
+
 # ------------------------------------------------------------------ work split across CTA pairs
 @pytest.mark.parametrize("name", ["ragged_bf16_cur", "mtp_fp16", "heads16_fp32part"])
 def test_whole_shards_without_workspace(name):
