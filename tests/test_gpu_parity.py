@@ -223,6 +223,22 @@ def test_many_query_tokens_few_heads():
     assert_out_close(f64(out), ref_out, "out")
 
 
+def test_all_parts_empty():
+    """No history and no CURRENT chunk: every partial is o = 0, lse = -inf,
+    and the combined output is 0 (with and without a workspace)."""
+    cfg = inputs.DecodeConfig(name="em", batch=3, heads=128, q_len=1, num_shards=4,
+                              block_size=32, ragged=(1, 100), current=False, seed=131)
+    dp = DeviceProblem(inputs.make_problem(cfg, seq_lens=[0, 0, 0]))
+    for ws in ("default", None):
+        o_part, lse_part = dp.partial(workspace=ws)
+        out = api.mla_lse_combine_vup(o_part, lse_part, dp.W, err_flag=dp.err)
+        torch.cuda.synchronize()
+        assert dp.err.item() == 0
+        assert torch.isneginf(lse_part).all()
+        assert not o_part.float().abs().sum().item()
+        assert not out.float().abs().sum().item()
+
+
 # ------------------------------------------------------------------ work split across CTA pairs
 @pytest.mark.parametrize("name", ["ragged_bf16_cur", "mtp_fp16", "heads16_fp32part"])
 def test_whole_shards_without_workspace(name):
