@@ -208,6 +208,24 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ our arm
+def max_over_ranks(values, world: int, device="cpu"):
+    """Each timing's maximum over the ranks: N replicas take as long as the
+    slowest one.  Collective over the default process group when world > 1."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replica_throughput(world: int, units_per_replica: float, ms_per_step: float) -> float:
+    """Whole-job rate of N replicas: every rank's units over the slowest rank's
+    time per step (weak scaling)."""
+    return world * units_per_replica / (ms_per_step * 1e-3)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -320,17 +338,14 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = f0.elapsed_time(f1)
     clocks = ClockSampler.summarize(sampler.stop(), w0, w1) if sampler else None
 
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_ms, partial_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms, partial_ms = t.tolist()
+    total_ms, e2e_ms, partial_ms = max_over_ranks([total_ms, e2e_ms, partial_ms], world, dev)
     if rank != 0:
         return None
 
     ms_per_step = total_ms / args.steps
-    kv_tbs = world * wm["kv_bytes"] / (ms_per_step * 1e-3) / 1e12
-    tok_s = world * wm["query_tokens"] / (ms_per_step * 1e-3)
-    e2e_tbs = world * wm["kv_bytes"] / (e2e_ms / args.steps * 1e-3) / 1e12
+    kv_tbs = replica_throughput(world, wm["kv_bytes"], ms_per_step) / 1e12
+    tok_s = replica_throughput(world, wm["query_tokens"], ms_per_step)
+    e2e_tbs = replica_throughput(world, wm["kv_bytes"], e2e_ms / args.steps) / 1e12
     peaks, peak_src = load_peaks()
     part_s = partial_ms * 1e-3
     hbm_ach = wm["partial_bytes"] / part_s / 1e9
