@@ -113,8 +113,9 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
   const int box_v = block_size < mla::kPartialBoxV ? block_size : mla::kPartialBoxV;
   const uint64_t qrows = static_cast<uint64_t>(B) * q_len * H;
   const uint64_t kv_rows = static_cast<uint64_t>(num_blocks) * block_size;
-  CUtensorMap tm_qpe, tm_kv, tm_cur, tm_kv_v, tm_cur_v;
-  if (!make_map(&tm_qpe, q_pe, 64, qrows, 128, 64, 128, bf16) ||
+  CUtensorMap tm_qlat, tm_qpe, tm_kv, tm_cur, tm_kv_v, tm_cur_v;
+  if (!make_map(&tm_qlat, q_abs, 512, qrows, 1024, 64, 128, bf16) ||
+      !make_map(&tm_qpe, q_pe, 64, qrows, 128, 64, 128, bf16) ||
       !make_map(&tm_kv, kv_cache, 576, kv_rows, 1152, 64, box_k, bf16) ||
       !make_map(&tm_kv_v, kv_cache, 576, kv_rows, 1152, 64, box_v, bf16))
     return MLA_ERR_CUDA;
@@ -166,7 +167,7 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
     pp.ws_lse = reinterpret_cast<float*>(w + recs);
     pp.ws_o = w + recs + 2 * static_cast<size_t>(clusters) * 128 * 4;
   }
-  return launched(mla::launch_partial(tm_qpe, tm_kv, tm_cur, tm_kv_v, tm_cur_v, q_abs, pp, bf16,
+  return launched(mla::launch_partial(tm_qlat, tm_qpe, tm_kv, tm_cur, tm_kv_v, tm_cur_v, pp, bf16,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 

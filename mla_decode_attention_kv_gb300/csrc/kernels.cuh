@@ -43,8 +43,8 @@ int partial_max_clusters();
 constexpr int kPartialBoxK = 128;
 constexpr int kPartialBoxV = 32;
 
-int launch_partial(const CUtensorMap& qpe, const CUtensorMap& kv, const CUtensorMap& cur,
-                   const CUtensorMap& kv_v, const CUtensorMap& cur_v, const void* q_abs,
+int launch_partial(const CUtensorMap& qlat, const CUtensorMap& qpe, const CUtensorMap& kv,
+                   const CUtensorMap& cur, const CUtensorMap& kv_v, const CUtensorMap& cur_v,
                    const PartialParams& pp, bool bf16, cudaStream_t stream);
 int launch_combine(const void* o_part, const float* lse_part, int P, const void* o_local,
                    const float* lse_local, int T, int H, int part_dt, int out_dt, void* o_latent,

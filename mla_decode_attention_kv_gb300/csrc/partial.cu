@@ -214,12 +214,12 @@ static_assert((B_COUNT + 1) * 8 + 8 + 16 <= 512, "barrier block");
 
 template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
-    mla_partial_kernel(const __grid_constant__ CUtensorMap tm_qpe,
+    mla_partial_kernel(const __grid_constant__ CUtensorMap tm_qlat,
+                       const __grid_constant__ CUtensorMap tm_qpe,
                        const __grid_constant__ CUtensorMap tm_kv,
                        const __grid_constant__ CUtensorMap tm_cur,
                        const __grid_constant__ CUtensorMap tm_kv_v,
-                       const __grid_constant__ CUtensorMap tm_cur_v, const uint16_t* __restrict__ q_abs,
-                       const PartialParams pp) {
+                       const __grid_constant__ CUtensorMap tm_cur_v, const PartialParams pp) {
   using L = PairSmem;
   constexpr int TILE = L::kTile;
   constexpr int kTmemCols = 512;
@@ -280,6 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_qlat);
     prefetch_tmap(&tm_qpe);
     prefetch_tmap(&tm_kv);
     prefetch_tmap(&tm_cur);
@@ -482,11 +483,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         nx.advance(pp);
         const int id_next = boxlane ? fetch_id(nx, br_k, lane) : 0;
         const int row = boxlane ? box_row(it, br_k, lane, id_cur) : 0;
-        if (it.first() && it.newq) {
+        const bool newq = it.first() && it.newq;
+        const int qrow = (ui.b * pp.q_len + ui.i) * pp.H;
+        if (newq) {
+          // Q latent of the new query: eight 64-column chunks through the
+          // ring, ahead of the unit's K (the softmax warps move them to TMEM)
+          for (int c = 0; c < 8; ++c) {
+            const int st = cs % L::kNK;
+            if (cs >= L::kNK && !wait(&bar[B_KEMPTY + st], ((cs / L::kNK) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&bar[B_KFULL + st], L::kKStage);
+              tma_load_2d(sK + st * L::kKStage, &tm_qlat, &bar[B_KFULL + st], c * 64, qrow, pol_q);
+            }
+            ++cs;
+          }
+          if (!ok) break;
+          // Q RoPE tile: its buffer is free once the previous query's MMAs are done
           if (it.nq >= 1 && !wait(&bar[B_Q_EMPTY], (it.nq - 1) & 1)) break;
           if (lane == 0) {
             mbar_arrive_expect_tx(&bar[B_QR_FULL], 16384);
-            tma_load_2d(sQr, &tm_qpe, &bar[B_QR_FULL], 0, (ui.b * pp.q_len + ui.i) * pp.H, pol_q);
+            tma_load_2d(sQr, &tm_qpe, &bar[B_QR_FULL], 0, qrow, pol_q);
           }
           ++qloads;
         }
@@ -531,6 +550,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
               ok = false;
               break;
             }
+            cs += 8;   // the Q latent chunks in the ring are the softmax warps' to free
           }
           const int sb = g & 1;
           if (g >= 2 && !wait(&bar[B_S_EMPTY + sb], ((g >> 1) - 1) & 1)) { ok = false; break; }
@@ -579,40 +599,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       TileIter<TILE> it;
       it.start(pp, rng);
       int g = 0;
+      int cq = 0;   // ring position: 8 Q chunks per new query, 9 K chunks per tile
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       while (ok && it.valid) {
         const UnitInfo ui = it.ui;
         if (it.first()) {
           if (it.newq) {
-            // Q latent row r -> TMEM (packed pairs, low half = even element)
+            // Q latent row r -> TMEM (packed pairs, low half = even element),
+            // from the eight ring stages the producer filled for this query
             // (the softmax warps meet at named barriers, so every exit
             // decision is made together through named_bar_and)
             const bool qe = it.nq < 1 || wait_lazy(&bar[B_Q_EMPTY], (it.nq - 1) & 1);
             if (!named_bar_and(1, 128, qe)) { ok = false; break; }
             tc_fence_after();
-            const uint4* src = reinterpret_cast<const uint4*>(
-                q_abs + (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.H + r) * 512);
-            // two passes of 32 independent 16-byte loads (half a row each)
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-              uint4 x[32];
-#pragma unroll
-              for (int v = 0; v < 32; ++v)
-                x[v] = r < pp.H ? __ldg(src + half * 32 + v) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                uint32_t w[32];
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                  w[4 * v] = x[k * 8 + v].x;
-                  w[4 * v + 1] = x[k * 8 + v].y;
-                  w[4 * v + 2] = x[k * 8 + v].z;
-                  w[4 * v + 3] = x[k * 8 + v].w;
-                }
-                tmem_st32(tmem + lane_base + kQlatCol + (half * 4 + k) * 32, w);
+            for (int c = 0; c < 8; ++c) {
+              const int st = cq % L::kNK;
+              if (!named_bar_and(1, 128, wait_lazy(&bar[B_KFULL + st], (cq / L::kNK) & 1))) {
+                ok = false;
+                break;
               }
+              // row r of a 128-byte-swizzled stage: 16-byte unit j at (j ^ (r & 7))
+              const uint8_t* rowp = sK + st * L::kKStage + r * 128;
+              uint32_t w[32];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                uint4 x = *reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4));
+                if (r >= pp.H) x = make_uint4(0, 0, 0, 0);   // rows of the next query
+                w[4 * j] = x.x;
+                w[4 * j + 1] = x.y;
+                w[4 * j + 2] = x.z;
+                w[4 * j + 3] = x.w;
+              }
+              named_bar_sync(1, 128);   // every row of the stage is in registers
+              if (threadIdx.x == 128) mbar_arrive(&bar[B_KEMPTY + st]);
+              tmem_st32(tmem + lane_base + kQlatCol + c * 32, w);
+              ++cq;
             }
+            if (!ok) break;
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -709,6 +733,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         ok = named_bar_and(1, 128, ok && !*abort_flag);
         it.advance(pp);
         ++g;
+        cq += 9;
       }
       if (threadIdx.x == 128) bulk_wait_read<0>();
     }
@@ -1094,16 +1119,17 @@ int partial_max_clusters() {
 }
 
 template <bool BF16>
-static int launch_partial_t(const CUtensorMap& qpe, const CUtensorMap& kv, const CUtensorMap& cur,
-                            const CUtensorMap& kv_v, const CUtensorMap& cur_v,
-                            const uint16_t* q_abs, const PartialParams& pp, cudaStream_t stream) {
+static int launch_partial_t(const CUtensorMap& qlat, const CUtensorMap& qpe, const CUtensorMap& kv,
+                            const CUtensorMap& cur, const CUtensorMap& kv_v,
+                            const CUtensorMap& cur_v, const PartialParams& pp,
+                            cudaStream_t stream) {
   int max_clusters = 0;
   if (prepare_partial<BF16>(&max_clusters) != 0) return -1;
   // with a workspace every resident pair takes an equal share of the tiles
   const int clusters = pp.split ? pp.split : std::max(1, std::min(pp.num_units, max_clusters));
   if (clusters > max_clusters) return -1;
   mla_partial_kernel<BF16><<<dim3(2 * clusters), dim3(256), PairSmem::kTotal, stream>>>(
-      qpe, kv, cur, kv_v, cur_v, q_abs, pp);
+      qlat, qpe, kv, cur, kv_v, cur_v, pp);
   if (pp.split) {
     // programmatic dependent launch: the merge grid is scheduled while the
     // partial grid drains and waits for it on the device (griddepcontrol)
@@ -1122,12 +1148,11 @@ static int launch_partial_t(const CUtensorMap& qpe, const CUtensorMap& kv, const
   return 0;
 }
 
-int launch_partial(const CUtensorMap& qpe, const CUtensorMap& kv, const CUtensorMap& cur,
-                   const CUtensorMap& kv_v, const CUtensorMap& cur_v, const void* q_abs,
+int launch_partial(const CUtensorMap& qlat, const CUtensorMap& qpe, const CUtensorMap& kv,
+                   const CUtensorMap& cur, const CUtensorMap& kv_v, const CUtensorMap& cur_v,
                    const PartialParams& pp, bool bf16, cudaStream_t stream) {
-  const uint16_t* q = static_cast<const uint16_t*>(q_abs);
-  return bf16 ? launch_partial_t<true>(qpe, kv, cur, kv_v, cur_v, q, pp, stream)
-              : launch_partial_t<false>(qpe, kv, cur, kv_v, cur_v, q, pp, stream);
+  return bf16 ? launch_partial_t<true>(qlat, qpe, kv, cur, kv_v, cur_v, pp, stream)
+              : launch_partial_t<false>(qlat, qpe, kv, cur, kv_v, cur_v, pp, stream);
 }
 
 }  // namespace mla

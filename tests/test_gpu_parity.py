@@ -239,6 +239,36 @@ def test_all_parts_empty():
         assert not out.float().abs().sum().item()
 
 
+@pytest.mark.parametrize("name", ["ragged_bf16_cur", "heads16_fp32part"])
+def test_partials_at_16_byte_offsets(name):
+    """q_abs, q_pe and o_part 16-byte aligned but not 32-byte aligned: the
+    TMA maps take any 16-byte base and the epilogue falls back from its
+    32-byte stores; same results."""
+    dp = DeviceProblem(inputs.make_problem(SMALL[name]))
+
+    def shifted(t, dtype=None):
+        dtype = dtype or t.dtype
+        pad = 16 // torch.empty((), dtype=dtype).element_size()
+        buf = torch.empty(t.numel() + pad, dtype=dtype, device=t.device)
+        out = buf[pad:].view(t.shape)
+        assert out.data_ptr() % 32 == 16
+        return out
+
+    dp.q_abs = shifted(dp.q_abs).copy_(dp.q_abs)
+    dp.q_pe = shifted(dp.q_pe).copy_(dp.q_pe)
+    cfg = dp.prob.cfg
+    P = cfg.num_shards + (1 if cfg.current else 0)
+    o_part = shifted(torch.empty((cfg.batch, cfg.q_len, P, cfg.heads, 512), dtype=dp.part_dt,
+                                 device=dp.dev))
+    for ws in ("default", None):
+        o_part.fill_(float("nan"))
+        o, lse_part = dp.partial(o_part=o_part, workspace=ws)
+        torch.cuda.synchronize()
+        assert o.data_ptr() == o_part.data_ptr()
+        assert dp.err.item() == 0
+        _check_partials(dp, o, lse_part)
+
+
 # ------------------------------------------------------------------ work split across CTA pairs
 @pytest.mark.parametrize("name", ["ragged_bf16_cur", "mtp_fp16", "heads16_fp32part"])
 def test_whole_shards_without_workspace(name):
