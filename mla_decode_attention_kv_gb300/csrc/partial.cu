@@ -209,8 +209,9 @@ enum : int {
   B_MMA_DONE_B = B_O_FIXED + 1,
   B_COUNT = B_MMA_DONE_B + 1
 };
-// barriers + TMEM slot + abort flag + 4 warp flags must fit the barrier block
-static_assert((B_COUNT + 1) * 8 + 8 + 16 <= 512, "barrier block");
+// barriers + TMEM slot + abort flag + 4 warp flags + 8 Q-chunk counters must
+// fit the barrier block
+static_assert((B_COUNT + 4) * 8 + 32 <= 512, "barrier block");
 
 template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
@@ -234,6 +235,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + B_COUNT + 1);
   volatile uint32_t* warp_flags = reinterpret_cast<volatile uint32_t*>(bar + B_COUNT + 2);
+  int* q_readers = reinterpret_cast<int*>(bar + B_COUNT + 4);   // warps done with Q chunk c
 
   const uint32_t rank = cluster_ctarank();
   const int warp = threadIdx.x >> 5;
@@ -255,6 +257,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         mbar_init(&bar[B_PFREE + k], 1);
       }
       mbar_init(&bar[B_MMA_DONE_A], 1);
+      for (int c = 0; c < 8; ++c) q_readers[c] = 0;
     } else {
       for (int s = 0; s < L::kNV; ++s) {
         mbar_init(&bar[B_VFULL + s], 1);
@@ -482,10 +485,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         TileIter<TILE> nx = it;
         nx.advance(pp);
         const int id_next = boxlane ? fetch_id(nx, br_k, lane) : 0;
-        const int row = boxlane ? box_row(it, br_k, lane, id_cur) : 0;
-        const bool newq = it.first() && it.newq;
-        const int qrow = (ui.b * pp.q_len + ui.i) * pp.H;
-        if (newq) {
+        if (it.first() && it.newq) {
+          const int qrow = (ui.b * pp.q_len + ui.i) * pp.H;
           // Q latent of the new query: eight 64-column chunks through the
           // ring, ahead of the unit's K (the softmax warps move them to TMEM)
           for (int c = 0; c < 8; ++c) {
@@ -509,6 +510,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           }
           ++qloads;
         }
+        // (after the Q loads: the box rows wait for the block-table entries)
+        const int row = boxlane ? box_row(it, br_k, lane, id_cur) : 0;
         const CUtensorMap* map = ui.current ? &tm_cur : &tm_kv;
         uint8_t* dst = sK + lane * br_k * 128;
         for (int c = 0; c < 9; ++c) {
@@ -613,9 +616,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             const bool qe = it.nq < 1 || wait_lazy(&bar[B_Q_EMPTY], (it.nq - 1) & 1);
             if (!named_bar_and(1, 128, qe)) { ok = false; break; }
             tc_fence_after();
+            // each warp copies its 32 rows of a chunk; the last warp done
+            // with a chunk frees its stage (no block-wide barrier per chunk)
             for (int c = 0; c < 8; ++c) {
-              const int st = cq % L::kNK;
-              if (!named_bar_and(1, 128, wait_lazy(&bar[B_KFULL + st], (cq / L::kNK) & 1))) {
+              const int st = (cq + c) % L::kNK;
+              if (!wait_lazy(&bar[B_KFULL + st], ((cq + c) / L::kNK) & 1)) {
                 ok = false;
                 break;
               }
@@ -631,12 +636,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 w[4 * j + 2] = x.z;
                 w[4 * j + 3] = x.w;
               }
-              named_bar_sync(1, 128);   // every row of the stage is in registers
-              if (threadIdx.x == 128) mbar_arrive(&bar[B_KEMPTY + st]);
-              tmem_st32(tmem + lane_base + kQlatCol + c * 32, w);
-              ++cq;
+              tmem_st32(tmem + lane_base + kQlatCol + c * 32, w);   // consumes the loads
+              __syncwarp();
+              if (lane == 0) {
+                __threadfence_block();
+                if (atomicAdd(&q_readers[c], 1) == 3) {
+                  q_readers[c] = 0;
+                  mbar_arrive(&bar[B_KEMPTY + st]);
+                }
+              }
             }
-            if (!ok) break;
+            cq += 8;
+            if (!named_bar_and(1, 128, ok)) { ok = false; break; }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
