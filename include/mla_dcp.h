@@ -210,11 +210,20 @@ int mla_vup(const void* o_latent, const void* W_UV, int T, int H, int dtype, voi
             int32_t* err_flag, mla_stream_t stream);
 
 /*
- * mla_lse_combine_vup -- mla_lse_combine and mla_vup in one launch.  The
- * combined latent of each head is rounded to `dtype` and fed straight to the
- * up-projection from on-chip memory.  Arguments as in the two calls above;
- * o_latent (written too, if non-NULL) and out use `dtype`.
- *   1 <= T <= 65536 (rows are processed in tiles of 64)
+ * mla_lse_combine_vup -- mla_lse_combine and mla_vup in one launch.  Two
+ * exact forms of the same result ([PR] code block A: combine, then the
+ * batch-major V-up), chosen per call:
+ *   - partials in `dtype` (part_dtype == dtype), at most 64 parts counting
+ *     o_local, o_latent NULL: every part's rows are up-projected on the
+ *     tensor cores and the LSE-weighted sum is taken in fp32 in the 128-wide
+ *     V space (the projection is linear), so the combined latent is never
+ *     rounded;
+ *   - otherwise: the combined latent of each head is rounded to `dtype` and
+ *     fed to the up-projection from on-chip memory.
+ * Arguments as in the two calls above; o_latent (written too, if non-NULL)
+ * and out use `dtype`.  Parts with lse = -inf are skipped whatever their
+ * rows hold.
+ *   1 <= T <= 65536
  */
 int mla_lse_combine_vup(const void* o_part, const float* lse_part, int num_parts,
                         const void* o_local, const float* lse_local, const void* W_UV, int T,

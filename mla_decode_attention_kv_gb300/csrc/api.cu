@@ -45,6 +45,22 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over [d2, d1, 512] 16-bit elements (row strides in bytes) with a
+// box of 64 x 1 x box_d2 and 128-byte swizzle: box_d2 rows of one (d1) slice.
+bool make_map_3d(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2, uint64_t stride1,
+                 uint64_t stride2, uint32_t box_d2, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {512, d1, d2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {64, 1, box_d2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool is_half_dtype(int d) { return d == MLA_BF16 || d == MLA_FP16; }
 bool is_part_dtype(int d) { return d == MLA_BF16 || d == MLA_FP16 || d == MLA_FP32; }
@@ -246,6 +262,21 @@ static int vup_common(bool combine, const void* o_part, const float* lse_part, i
   if (T < 1 || T > 65536 || H < 1 || H > MLA_MAX_HEADS) return MLA_ERR_BAD_SHAPE;
   if (!aligned16(W_UV) || !aligned16(out)) return MLA_ERR_MISALIGNED;
   const bool bf16 = dtype == MLA_BF16;
+  const int nparts = num_parts + (o_local ? 1 : 0);
+  if (combine && part_dtype == dtype && nparts <= mla::kVupPartsMax && !o_latent_out) {
+    // partials in W_UV's dtype: the V-up of every part, then the weighted sum
+    const mla::VupPartsPlan plan = mla::vup_parts_plan(nparts, T);
+    const uint64_t row = 1024;   // one 512-element latent row
+    CUtensorMap tm_w64, tm_p, tm_l;
+    if (!make_map(&tm_w64, W_UV, 128, static_cast<uint64_t>(H) * 512, 256, 64, 64, bf16) ||
+        !make_map_3d(&tm_p, o_part, static_cast<uint64_t>(num_parts) * H, T, row,
+                     row * num_parts * H, plan.tb, bf16) ||
+        !make_map_3d(&tm_l, o_local ? o_local : o_part, H, T, row, row * H, plan.tb, bf16))
+      return MLA_ERR_CUDA;
+    return launched(mla::launch_vup_parts(tm_w64, tm_p, tm_l, plan, bf16, T, H, num_parts,
+                                          o_local != nullptr, lse_part, lse_local, out, lse_out,
+                                          err_flag, reinterpret_cast<cudaStream_t>(stream)));
+  }
   CUtensorMap tm_w;
   if (!make_map(&tm_w, W_UV, 128, static_cast<uint64_t>(H) * 512, 256, 64, 256, bf16))
     return MLA_ERR_CUDA;

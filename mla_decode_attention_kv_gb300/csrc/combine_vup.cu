@@ -18,6 +18,13 @@
 // TMA-loaded), B = the latent rows of head h (N = rows of a 64-row tile,
 // K-major in shared memory), D in TMEM.  In the fused form the combine writes
 // its bf16/fp16 result for head h directly into that B operand.
+//
+// When the partials are stored in W_UV's dtype the fused call instead takes
+// the up-projection of every part and the LSE-weighted sum afterwards, in the
+// 128-wide V space (the projection is linear):
+//   out[t, h] = sum_p w_p(t, h) * (o_p[t, h, :] . W_UV[h]),  w_p = exp(lse_p - LSE)
+// so the partials go from global memory to the tensor cores by TMA with no
+// pass through registers (mla_vup_parts_kernel).
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -343,6 +350,329 @@ __global__ void __launch_bounds__(256, 1)
     __syncwarp();
     tmem_dealloc(tmem, kVupRows);
   }
+}
+
+// ---------------------------------------------------------------- V-up of the parts
+// One CTA per head.  For each block of TB rows and each 64-wide K chunk the
+// producer stages W_UV[h]'s 64 rows (A, MN-major: two 64-column groups) and
+// the chunk of every part's TB rows (B, K-major: part p at B rows
+// [p*TB, p*TB + TB), rows past T zero-filled), and one elected thread issues
+//   D[v, p*TB + t] += sum_k W_UV[h][k, v] * o_p[t0 + t, h, k]
+// (M = 128, N = parts * TB in pieces of at most 256).  Warps 2-3 turn the
+// block's LSEs into weights; warps 4-7 (thread = v) read D and store
+//   out[t0 + t, h*128 + v] = sum_p w_p(t) * D[v, p*TB + t].
+struct VupPartsArgs {
+  int T, H, P, has_local;
+  const float* lse_part;
+  const float* lse_local;
+  void* out;
+  float* lse_out;
+  int* err;
+  int ns, stage_bytes, bn;
+};
+
+template <bool BF16, int TB>
+__global__ void __launch_bounds__(256, 1)
+    mla_vup_parts_kernel(const __grid_constant__ CUtensorMap tm_w,
+                         const __grid_constant__ CUtensorMap tm_p,
+                         const __grid_constant__ CUtensorMap tm_l, const VupPartsArgs va) {
+  constexpr int kChunks = 512 / 64;
+  constexpr int kWChunk = 16384;               // 64 k-rows x 128 v, two 8 KB column groups
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t bar_full[4], bar_empty[4], bar_d_full, bar_d_empty,
+      bar_wt_full[2], bar_wt_empty[2], bar_mma_done;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int s_abort;
+  __shared__ float s_lse[512];     // LSE of part p, row t of the block: [p * TB + t]
+  __shared__ float s_w[2][512];    // weights of the block, double-buffered
+  const int h = blockIdx.x;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int np = va.P + va.has_local;
+  const int nblk = (va.T + TB - 1) / TB;
+  const int total = nblk * kChunks;
+  volatile int* abort_flag = &s_abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < va.ns; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    mbar_init(&bar_d_full, 1);
+    mbar_init(&bar_d_empty, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_wt_full[b], 1);
+      mbar_init(&bar_wt_empty[b], 4);
+    }
+    mbar_init(&bar_mma_done, 1);
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  int ncols = 32;
+  while (ncols < va.bn) ncols <<= 1;
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, ncols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_p);
+    prefetch_tmap(&tm_l);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  auto wait = [&](uint64_t* b, uint32_t parity) -> bool {
+    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+      if (mbar_try_wait(b, parity)) return true;
+      if ((it & 1023u) == 1023u && *abort_flag) return false;
+    }
+    set_error(va.err, kDevWaitTimeout);
+    *abort_flag = 1;
+    return false;
+  };
+  auto wait_lazy = [&](uint64_t* b, uint32_t parity) -> bool {
+    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+      if (mbar_try_wait_sleep(b, parity, kLazyWaitNs)) return true;
+      if ((it & 15u) == 15u && *abort_flag) return false;
+    }
+    set_error(va.err, kDevWaitTimeout);
+    *abort_flag = 1;
+    return false;
+  };
+  const uint32_t stage_tx = kWChunk + static_cast<uint32_t>(np * TB * 128);
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer (converged warp)
+    const uint64_t pol_w = nblk > 1 ? policy_evict_last() : policy_evict_first();
+    const uint64_t pol_p = policy_evict_first();
+    auto issue_w = [&](int q) {
+      const int s = q % va.ns;
+      uint8_t* st = smem + s * va.stage_bytes;
+      const int k0 = h * 512 + (q % kChunks) * 64;
+      mbar_arrive_expect_tx(&bar_full[s], stage_tx);
+      tma_load_2d(st, &tm_w, &bar_full[s], 0, k0, pol_w);
+      tma_load_2d(st + kWChunk / 2, &tm_w, &bar_full[s], 64, k0, pol_w);
+    };
+    // W_UV does not depend on the previous grid: the first stages' W before
+    // the wait for the grid that wrote the partials
+    const int pre = min(va.ns, total);
+    if (lane == 0)
+      for (int q = 0; q < pre; ++q) issue_w(q);
+    __syncwarp();
+    griddep_wait();
+    int q = 0;
+    for (; q < total; ++q) {
+      const int s = q % va.ns;
+      if (q >= va.ns) {
+        if (!wait(&bar_empty[s], ((q / va.ns) - 1) & 1)) break;
+        if (lane == 0) issue_w(q);
+        __syncwarp();
+      }
+      uint8_t* st = smem + s * va.stage_bytes + kWChunk;
+      const int c = q % kChunks, t0 = (q / kChunks) * TB;
+      for (int p = lane; p < np; p += 32) {
+        if (p < va.P)
+          tma_load_3d(st + p * TB * 128, &tm_p, &bar_full[s], c * 64, p * va.H + h, t0, pol_p);
+        else
+          tma_load_3d(st + p * TB * 128, &tm_l, &bar_full[s], c * 64, h, t0, pol_p);
+      }
+    }
+    // drain: W is in flight for every stage armed so far
+    const int armed = max(q, pre);
+    if (lane == 0)
+      for (int s = 0; s < va.ns && s < armed; ++s) {
+        const int last = armed - 1 - ((armed - 1 - s) % va.ns);
+        mbar_wait(&bar_full[s], (last / va.ns) & 1, va.err);
+      }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      int q = 0;
+      for (int blk = 0; blk < nblk && ok; ++blk) {
+        if (blk >= 1 && !wait(&bar_d_empty, (blk - 1) & 1)) break;
+        tc_fence_after();
+        for (int c = 0; c < kChunks; ++c, ++q) {
+          const int s = q % va.ns;
+          if (!wait(&bar_full[s], (q / va.ns) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t wa = smem_u32(smem + s * va.stage_bytes);
+          const uint32_t ba = wa + kWChunk;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = make_desc_sw128(wa + kk * 2048, kWChunk / 2, 1024);
+            for (int n0 = 0; n0 < va.bn; n0 += 256) {
+              const int n = min(256, va.bn - n0);
+              const uint64_t bd = make_desc_sw128(ba + n0 * 128 + kk * 32, 16, 1024);
+              umma_ss(tmem + n0, ad, bd, make_idesc_f16(128, n, BF16, true, false),
+                      (c | kk) ? 1u : 0u);
+            }
+          }
+          umma_commit(&bar_empty[s]);
+        }
+        if (ok) umma_commit(&bar_d_full);
+      }
+      umma_commit(&bar_mma_done);
+      mbar_wait(&bar_mma_done, 0, va.err);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------ LSE weights of each row block
+    const int wt = threadIdx.x - 64;
+    griddep_wait();
+    for (int blk = 0; blk < nblk; ++blk) {
+      const int b = blk & 1;
+      const int t0 = blk * TB;
+      const bool ok = blk < 2 || wait_lazy(&bar_wt_empty[b], ((blk >> 1) - 1) & 1);
+      if (!named_bar_and(2, 64, ok)) break;
+      for (int i = wt; i < np * TB; i += 64) {   // every LSE of the block at once
+        const int p = i / TB;
+        const int64_t t = t0 + i % TB;
+        float v = -INFINITY;
+        if (t < va.T)
+          v = p < va.P ? __ldg(va.lse_part + (t * va.P + p) * va.H + h)
+                       : __ldg(va.lse_local + t * va.H + h);
+        s_lse[i] = v;
+      }
+      named_bar_sync(2, 64);
+      for (int t = wt; t < TB; t += 64) {
+        float mx = -INFINITY;
+        for (int p = 0; p < np; ++p) mx = fmaxf(mx, s_lse[p * TB + t]);
+        float sum = 0.f;
+        for (int p = 0; p < np; ++p) {
+          const float v = s_lse[p * TB + t];
+          const float e = (mx == -INFINITY || v == -INFINITY) ? 0.f : __expf(v - mx);
+          s_w[b][p * TB + t] = e;
+          sum += e;
+        }
+        const float inv = sum > 0.f ? 1.f / sum : 0.f;
+        for (int p = 0; p < np; ++p) s_w[b][p * TB + t] *= inv;
+        if (va.lse_out && t0 + t < va.T)
+          va.lse_out[static_cast<int64_t>(t0 + t) * va.H + h] =
+              sum > 0.f ? mx + __logf(sum) : -INFINITY;
+      }
+      named_bar_sync(2, 64);
+      if (wt == 0) mbar_arrive(&bar_wt_full[b]);
+    }
+  } else {
+    // ------------------------------------------------ epilogue (thread = v)
+    const int wq = warp & 3;
+    const int v = wq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const int nvalid = np * TB;
+    uint16_t* o = static_cast<uint16_t*>(va.out);
+    griddep_wait();   // an earlier grid may still read out
+    for (int blk = 0; blk < nblk; ++blk) {
+      const int b = blk & 1;
+      const int t0 = blk * TB;
+      if (!wait_lazy(&bar_d_full, blk & 1) || !wait_lazy(&bar_wt_full[b], (blk >> 1) & 1)) break;
+      tc_fence_after();
+      float acc[TB];
+#pragma unroll
+      for (int t = 0; t < TB; ++t) acc[t] = 0.f;
+      const float* w = s_w[b];
+      for (int n0 = 0; n0 < nvalid; n0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + n0, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (n0 + i < nvalid) {
+            // a part of weight 0 (lse = -inf) is skipped, whatever its rows hold
+            const float wn = w[n0 + i];
+            acc[i % TB] += wn != 0.f ? wn * __uint_as_float(r[i]) : 0.f;
+          }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bar_d_empty);
+        mbar_arrive(&bar_wt_empty[b]);
+      }
+#pragma unroll
+      for (int t = 0; t < TB; ++t)
+        if (t0 + t < va.T)
+          o[(static_cast<int64_t>(t0 + t) * va.H + h) * 128 + v] =
+              static_cast<uint16_t>(pack2<BF16>(acc[t], 0.f) & 0xFFFFu);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, ncols);
+  }
+}
+
+VupPartsPlan vup_parts_plan(int num_parts, int T) {
+  VupPartsPlan pl = {};
+  pl.tb = num_parts <= 16 ? 32 : (num_parts <= 32 ? 16 : 8);
+  while (pl.tb > 8 && pl.tb / 2 >= T) pl.tb /= 2;
+  pl.bn = (num_parts * pl.tb + 15) / 16 * 16;
+  pl.stage_bytes = 16384 + pl.bn * 128;
+  // static shared memory of the kernel: about 6.3 KB; 1 KB for alignment
+  pl.ns = std::min(4, (232448 - 8192 - 1024) / pl.stage_bytes);
+  pl.tmem_cols = 32;
+  while (pl.tmem_cols < pl.bn) pl.tmem_cols <<= 1;
+  pl.smem_bytes = pl.ns * pl.stage_bytes + 1024;
+  return pl;
+}
+
+template <bool BF16, int TB>
+static int launch_vup_parts_t(const CUtensorMap& tm_w, const CUtensorMap& tm_p,
+                              const CUtensorMap& tm_l, const VupPartsPlan& plan,
+                              const VupPartsArgs& va, cudaStream_t stream) {
+  auto kern = mla_vup_parts_kernel<BF16, TB>;
+  static int configured[64] = {0};   // largest dynamic shared memory set per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  if (configured[dev] < plan.smem_bytes) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem_bytes) !=
+        cudaSuccess)
+      return -1;
+    configured[dev] = plan.smem_bytes;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(va.H, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = plan.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm_w, tm_p, tm_l, va) == cudaSuccess ? 0 : -1;
+}
+
+int launch_vup_parts(const CUtensorMap& tm_w64, const CUtensorMap& tm_p, const CUtensorMap& tm_l,
+                     const VupPartsPlan& plan, bool bf16, int T, int H, int P, bool has_local,
+                     const float* lse_part, const float* lse_local, void* out, float* lse_out,
+                     int* err, cudaStream_t stream) {
+  if (plan.ns < 2 || plan.bn > 512 || P + (has_local ? 1 : 0) > kVupPartsMax) return -1;
+  VupPartsArgs va;
+  va.T = T;
+  va.H = H;
+  va.P = P;
+  va.has_local = has_local ? 1 : 0;
+  va.lse_part = lse_part;
+  va.lse_local = lse_local;
+  va.out = out;
+  va.lse_out = lse_out;
+  va.err = err;
+  va.ns = plan.ns;
+  va.stage_bytes = plan.stage_bytes;
+  va.bn = plan.bn;
+#define MLA_VP(B, TBV) launch_vup_parts_t<B, TBV>(tm_w64, tm_p, tm_l, plan, va, stream)
+  switch (plan.tb) {
+    case 32: return bf16 ? MLA_VP(true, 32) : MLA_VP(false, 32);
+    case 16: return bf16 ? MLA_VP(true, 16) : MLA_VP(false, 16);
+    case 8: return bf16 ? MLA_VP(true, 8) : MLA_VP(false, 8);
+    default: return -1;
+  }
+#undef MLA_VP
 }
 
 // ---------------------------------------------------------------- launchers

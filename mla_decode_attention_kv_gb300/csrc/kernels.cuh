@@ -53,6 +53,22 @@ int launch_vup(const CUtensorMap& tm_w, bool combine, bool bf16, const void* o_p
                const float* lse_part, int P, const void* o_local, const float* lse_local,
                const void* o_latent_in, int T, int H, int part_dt, void* out, void* o_latent_out,
                float* lse_out, int* err, cudaStream_t stream);
+// mla_lse_combine_vup through the V-up of every part (partials in the
+// storage dtype, at most kVupPartsMax parts): the row block and ring plan.
+constexpr int kVupPartsMax = 64;
+struct VupPartsPlan {
+  int tb;            // rows per block: 8, 16 or 32
+  int bn;            // B rows per K chunk: parts * tb rounded up to 16
+  int stage_bytes;   // W chunk (16 KB) + B chunk
+  int ns;            // ring stages
+  int tmem_cols;
+  int smem_bytes;    // dynamic shared memory
+};
+VupPartsPlan vup_parts_plan(int num_parts, int T);
+int launch_vup_parts(const CUtensorMap& tm_w64, const CUtensorMap& tm_p, const CUtensorMap& tm_l,
+                     const VupPartsPlan& plan, bool bf16, int T, int H, int P, bool has_local,
+                     const float* lse_part, const float* lse_local, void* out, float* lse_out,
+                     int* err, cudaStream_t stream);
 int launch_gather(const void* kv_cache, const int32_t* block_table, const int32_t* seq_lens,
                   int B, int num_blocks, int bs, int max_blocks, int max_len, void* dst, int* err,
                   cudaStream_t stream);

@@ -102,6 +102,48 @@ def test_combine_dtypes_and_local(part, local):
     assert got_o.shape == (T, cfg.heads, 512)
 
 
+@pytest.mark.parametrize("P,local,T,H", [(7, True, 37, 8), (20, False, 5, 3), (40, True, 70, 2),
+                                         (64, False, 16, 4), (64, True, 9, 2)])
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_combine_vup_of_parts(P, local, T, H, dt):
+    """The fused combine + V-up with partials in W_UV's dtype (the up-projection
+    of every part, then the LSE-weighted sum): 1 to 9 blocks of rows, 8 to 65
+    parts (65 is past what that form takes and goes the register-combine way),
+    against combine-then-V-up in fp64.  An empty part (lse = -inf) holds NaN
+    rows that must not reach the output; row 0 of head 0 has no part at all."""
+    rng = np.random.default_rng(P * 1000 + T)
+    tdt = api.torch_dtype(dt)
+    o = rng.standard_normal((T, P, H, 512)).astype(np.float32)
+    lse = rng.uniform(-3.0, 3.0, (T, P, H)).astype(np.float32)
+    lse[:, 1, :] = -np.inf
+    o[:, 1] = np.nan
+    lse[0, :, 0] = -np.inf
+    W = (rng.standard_normal((H, 512, 128)) * 0.05).astype(np.float32)
+    o_t = torch.tensor(o).to(tdt).cuda()
+    lse_t = torch.tensor(lse).cuda()
+    W_t = torch.tensor(W).to(tdt).cuda()
+    kw = {}
+    o_loc = l_loc = None
+    if local:
+        o_loc = rng.standard_normal((T, H, 512)).astype(np.float32)
+        l_loc = rng.uniform(-3.0, 3.0, (T, H)).astype(np.float32)
+        l_loc[0, 0] = -np.inf
+        kw = dict(o_local=torch.tensor(o_loc).to(tdt).cuda(), lse_local=torch.tensor(l_loc).cuda())
+        o_loc = f64(kw["o_local"])
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lse_out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    out = api.mla_lse_combine_vup(o_t, lse_t, W_t, lse_out=lse_out, err_flag=err, **kw)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    ref_o, ref_l = om.lse_combine(np.nan_to_num(f64(o_t), nan=0.0), lse, o_loc, l_loc)
+    ref = om.v_up(ref_o, f64(W_t))
+    got = f64(out)
+    assert np.isfinite(got).all()
+    assert not got.reshape(T, H, 128)[0, 0].any()
+    assert_out_close(got, ref, "out")
+    assert_lse_close(f64(lse_out), ref_l, "lse_out")
+
+
 def test_vup_matches_oracle():
     rng = np.random.default_rng(5)
     for T, H in ((1, 1), (37, 8), (130, 128)):
