@@ -85,10 +85,9 @@ __device__ __forceinline__ UnitInfo unit_info(const PartialParams& pp, int u) {
 
 // Tile range of one cluster: tiles [j_begin, ...) of unit u_begin through
 // tiles [..., j_stop) of unit u_last, in the flat order of the units' tiles
-// (global tile index t_begin of the first one).  Units with no tiles whose
-// start falls in the cluster's share are [ue0, ue1).
+// (global tile index t_begin of the first one).
 struct TileRange {
-  int u_begin, j_begin, u_last, j_stop, t_begin, ue0, ue1;
+  int u_begin, j_begin, u_last, j_stop, t_begin;
 };
 
 // Walks the tiles of a TileRange as one flat stream.  A "piece" is the part
@@ -301,13 +300,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   // and the units at its ends may be split with the neighbouring clusters
   // (their pieces are merged through the workspace); without one the cluster
   // owns the whole units whose first tile falls in its share.  Units without
-  // tiles go to the cluster whose share holds their start.  Both CTAs of the
-  // pair compute the same range.
+  // tiles (o = 0, lse = -inf) are dealt round-robin: unit u to cluster
+  // u mod clusters, so a batch of short or empty histories spreads its zero
+  // rows over every pair.  Both CTAs of the pair compute the same range.
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(nclusters_x());
   __shared__ int s_scan[8];
   __shared__ int s_load[256];
-  __shared__ int s_rng[8];
+  __shared__ int s_rng[4];
   TileRange rng;
   int64_t share_total = 0;
   bool split = false;
@@ -340,8 +340,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       s_rng[1] = 0;         // j_begin
       s_rng[2] = -1;        // u_last
       s_rng[3] = 0;         // j_stop
-      s_rng[4] = U;         // ue0
-      s_rng[5] = U;         // ue1
     }
     for (int c = threadIdx.x; c < ncl; c += 256) s_load[c] = 0;
     __syncthreads();
@@ -376,8 +374,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     int64_t run = my_start;
     for (int u = a; u < e; ++u) {
       const int nt = unit_info<TILE>(pp, u).ntiles;
-      if (run >= lo) atomicMin(&s_rng[4], u);
-      if (run >= hi) atomicMin(&s_rng[5], u);
       if (nt > 0 && lo < hi) {
         if (split) {
           if (lo >= run && lo < run + nt) {
@@ -401,8 +397,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     rng.u_last = s_rng[2];
     rng.j_stop = split ? s_rng[3] : (rng.u_last >= 0 ? unit_info<TILE>(pp, rng.u_last).ntiles : 0);
     rng.t_begin = static_cast<int>(lo);
-    rng.ue0 = s_rng[4];
-    rng.ue1 = cid == ncl - 1 ? U : s_rng[5];
   }
 
   auto wait = [&](uint64_t* b, uint32_t parity) -> bool {
@@ -586,7 +580,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     } else if (warp == 2 || warp == 3) {
       // ------------------------------------------------ rank 0: LSE of empty parts
       const int t = threadIdx.x - 64;
-      for (int u = rng.ue0; u < rng.ue1; ++u) {
+      for (int u = cid; u < pp.num_units; u += ncl) {
         const UnitInfo ui = unit_info<TILE>(pp, u);
         if (ui.ntiles != 0) continue;
         const int64_t row0 = (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H;
@@ -863,7 +857,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       }
     } else if (warp == 3) {
       // ------------------------------------------------ rank 1: zeros of empty parts
-      for (int u = rng.ue0; u < rng.ue1; ++u) {
+      for (int u = cid; u < pp.num_units; u += ncl) {
         const UnitInfo ui = unit_info<TILE>(pp, u);
         if (ui.ntiles != 0) continue;
         const int64_t row0 = (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H;

@@ -265,14 +265,19 @@ def test_many_query_tokens_few_heads():
     assert_out_close(f64(out), ref_out, "out")
 
 
-def test_all_parts_empty():
+@pytest.mark.parametrize("batch,shards", [(3, 4), (32, 8), (5, 64)])
+def test_all_parts_empty(batch, shards):
     """No history and no CURRENT chunk: every partial is o = 0, lse = -inf,
-    and the combined output is 0 (with and without a workspace)."""
-    cfg = inputs.DecodeConfig(name="em", batch=3, heads=128, q_len=1, num_shards=4,
+    and the combined output is 0 (with and without a workspace).  The
+    outputs start as NaN, so a part that no CTA pair wrote would show."""
+    cfg = inputs.DecodeConfig(name="em", batch=batch, heads=128, q_len=1, num_shards=shards,
                               block_size=32, ragged=(1, 100), current=False, seed=131)
-    dp = DeviceProblem(inputs.make_problem(cfg, seq_lens=[0, 0, 0]))
+    dp = DeviceProblem(inputs.make_problem(cfg, seq_lens=[0] * batch))
     for ws in ("default", None):
-        o_part, lse_part = dp.partial(workspace=ws)
+        o_part = torch.full((batch, 1, shards, 128, 512), float("nan"), dtype=dp.part_dt,
+                            device=dp.dev)
+        lse_part = torch.full((batch, 1, shards, 128), float("nan"), device=dp.dev)
+        dp.partial(workspace=ws, o_part=o_part, lse_part=lse_part)
         out = api.mla_lse_combine_vup(o_part, lse_part, dp.W, err_flag=dp.err)
         torch.cuda.synchronize()
         assert dp.err.item() == 0
