@@ -297,30 +297,36 @@ def run_ours(args, rank, world, local_rank):
     if err.item() != 0:
         raise RuntimeError(f"device error {err.item()} during the timed region")
 
-    # ---- end to end through the public API with pinned host buffers
-    def pin(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    # ---- end to end through the public API with pinned host buffers.  The
+    # step's inputs are staged in one pinned buffer (each at a 256-byte
+    # aligned offset) and moved with one copy; the calls get device views.
+    parts = [("q_abs", prob.q_abs.view(np.int16)), ("q_pe", prob.q_pe.view(np.int16)),
+             ("table", prob.block_table), ("lens", prob.seq_lens)]
+    if prob.kv_cur is not None:
+        parts.append(("kv_cur", prob.kv_cur.view(np.int16)))
+    offs, off = {}, 0
+    for name, a in parts:
+        offs[name] = off
+        off += (a.nbytes + 255) // 256 * 256
+    h_in = torch.empty(off, dtype=torch.uint8).pin_memory()
+    for name, a in parts:
+        h_in[offs[name]:offs[name] + a.nbytes].copy_(
+            torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).reshape(-1)))
+    d_in = torch.empty(off, dtype=torch.uint8, device=dev)
+    wm["h2d_bytes"] = off   # what is copied: the inputs and their alignment padding
 
-    h_qa = pin(prob.q_abs.view(np.int16))
-    h_qp = pin(prob.q_pe.view(np.int16))
-    h_tab = pin(prob.block_table)
-    h_len = pin(prob.seq_lens)
-    h_cur = pin(prob.kv_cur.view(np.int16)) if prob.kv_cur is not None else None
+    def dview(name, like):
+        n = like.numel() * like.element_size()
+        return d_in[offs[name]:offs[name] + n].view(like.dtype).view(like.shape)
+
+    d_qa, d_qp = dview("q_abs", q_abs), dview("q_pe", q_pe)
+    d_tab, d_len = dview("table", table), dview("lens", lens)
+    d_cur = dview("kv_cur", kv_cur) if kv_cur is not None else None
     h_out = torch.empty((B * q, H * 128), dtype=torch.int16).pin_memory()
-    d_qa = torch.empty_like(q_abs)
-    d_qp = torch.empty_like(q_pe)
-    d_tab = torch.empty_like(table)
-    d_len = torch.empty_like(lens)
-    d_cur = torch.empty_like(kv_cur) if kv_cur is not None else None
 
     def e2e_step(i):
         li = i % layers
-        d_qa.view(torch.int16).copy_(h_qa, non_blocking=True)
-        d_qp.view(torch.int16).copy_(h_qp, non_blocking=True)
-        d_tab.copy_(h_tab, non_blocking=True)
-        d_len.copy_(h_len, non_blocking=True)
-        if d_cur is not None:
-            d_cur.view(torch.int16).copy_(h_cur, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         api.decode_step(d_qa, d_qp, caches[li], d_tab, d_len, Ws[li], cfg.num_shards,
                         kv_cur=d_cur, scale=cfg.scale, o_part=o_part, lse_part=lse_part,
                         out=out, err_flag=err, stream=stream)
