@@ -465,6 +465,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       // barrier and lane l issues box l of each chunk (no shuffles, no
       // divergent single-lane sections on the issue path).
       const uint64_t pol_kv = policy_evict_last();     // rank 1 re-reads the latent
+      const uint64_t pol_rope = policy_evict_first();  // chunk 8 (k_R): read once
       const uint64_t pol_q = policy_evict_last();
       TileIter<TILE> it;
       it.start(pp, rng);
@@ -516,7 +517,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           }
           if (lane == 0) mbar_arrive_expect_tx(&bar[B_KFULL + st], L::kKStage);
           if (boxlane)
-            tma_load_2d(dst + st * L::kKStage, map, &bar[B_KFULL + st], c * 64, row, pol_kv);
+            tma_load_2d(dst + st * L::kKStage, map, &bar[B_KFULL + st], c * 64, row,
+                        c < 8 ? pol_kv : pol_rope);
           ++cs;
         }
         if (!ok) break;
