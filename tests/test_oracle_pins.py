@@ -330,6 +330,37 @@ def test_vup_identity_blocks_and_head_order():
             assert np.array_equal(out[t, h * 128:(h + 1) * 128], (h + 1) * o[t, h, :128])
 
 
+def test_vup_of_parts_equals_combine_then_vup():
+    """The up-projection is linear, so projecting each part and taking the
+    LSE-weighted sum in the 128-wide V space equals combine-then-V-up (the
+    fused call's form for partials in the model dtype).  The per-part side
+    is written here with plain numpy: weights exp(lse_p - LSE), empty parts
+    (lse = -inf) weight 0, a row with no part gives 0."""
+    rng = np.random.default_rng(17)
+    T, P, H = 5, 6, 3
+    o = rng.standard_normal((T, P, H, 512))
+    lse = rng.uniform(-4.0, 4.0, (T, P, H))
+    lse[:, 2, :] = -np.inf
+    lse[1, :, 0] = -np.inf
+    W = rng.standard_normal((H, 512, 128)) * 0.05
+    o_c, l_c = om.lse_combine(o, lse)
+    want = om.v_up(o_c, W).reshape(T, H, 128)
+    got = np.zeros((T, H, 128))
+    for t in range(T):
+        for h in range(H):
+            fin = np.isfinite(lse[t, :, h])
+            if not fin.any():
+                continue
+            m = lse[t, fin, h].max()
+            w = np.where(fin, np.exp(np.where(fin, lse[t, :, h], m) - m), 0.0)
+            w /= w.sum()
+            for p in range(P):
+                if w[p]:
+                    got[t, h] += w[p] * (o[t, p, h] @ W[h])
+    assert not got[1, 0].any() and not want[1, 0].any()
+    assert np.max(np.abs(got - want)) < 1e-12 * max(1.0, np.abs(want).max())
+
+
 def test_shuffled_table_same_result_as_identity():
     base = inputs.DecodeConfig(name="p", batch=2, heads=2, q_len=1, num_shards=3,
                                block_size=8, history=50, seed=4)
