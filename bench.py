@@ -1,16 +1,21 @@
 """Benchmark of one decode step of MLA attention over a sharded latent KV cache.
 
 A step is the whole hot path on one batch: the per-shard partial attention
-kernel, then the fused LSE combine + V-up kernel.  The default workload is
-the DeepSeek-V3-shaped decode (batch 32, 128 heads, 4096 history tokens per
-sequence in 8 shards, 64-token pages with a shuffled block table, bf16).
+kernel (with its split-shard merge), then the fused LSE combine + V-up
+kernel.  The default workload is the very long context decode (batch 16,
+128 heads, 131072 history tokens per sequence in 16 shards, 64-token pages
+with a shuffled block table, bf16, 2.4 GB of latent KV per layer): the
+largest single-GPU workload, and one of those at L >= 32K.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config NAME] [--extra NAMES|none]
 
 Prints one JSON line (rank 0).  `value` is the KV-read rate in TB/s: the
 latent-KV bytes every step must read, divided by the device time per step.
 Inputs are larger than L2: each step uses the next of several layer caches
-(and W_UV copies), so no step finds the previous step's KV in L2.
+(and W_UV copies), so no step finds the previous step's KV in L2.  The
+other workloads (--extra) are timed the same way, device-only, and reported
+under "extra_workloads".
 
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
 workload on this machine's host cores (the CPU baseline arm).
@@ -43,7 +48,7 @@ from mla_decode_attention_kv_gb300 import inputs  # noqa: E402
 
 METRIC = "MLA decode attn: KV-read TB/s, tokens/s, % of roofline at 1 GB300"
 L2_BYTES = 129 * 2 ** 20
-PROFILE = os.path.join(ROOT, "profiles", "partial_kernel_dsv3.md")
+PROFILES = os.path.join(ROOT, "profiles")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 WORKLOAD_TEXT = {
@@ -122,24 +127,29 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
+def profile_counters(config_name: str):
+    """The committed ncu counters of the partial kernel on this workload
+    (profiles/partial_kernel_<config>.json), if they were taken on the
+    current kernel source; else None."""
+    try:
+        with open(os.path.join(PROFILES, f"partial_kernel_{config_name}.json")) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    return d
+
+
 def traffic_from_profile(config_name: str):
-    """DRAM bytes per launch of the partial kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
-    try:
-        text = open(PROFILE).read()
-    except OSError:
+    """DRAM bytes (read + write) per launch of the partial kernel, scaled to
+    a full launch when the capture was taken on a smaller case; else None."""
+    d = profile_counters(config_name)
+    if not d:
         return None
-    fields = {}
-    for line in text.splitlines():
-        if line.startswith("- ") and ":" in line:
-            k, v = line[2:].split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
-    if fields.get("kernel_source_sha") != kernel_source_sha():
-        return None
-    key = f"dram_bytes_per_launch_{config_name}"
     try:
-        return float(fields[key])
-    except (KeyError, ValueError):
+        return float(d["dram_bytes_per_launch"])
+    except (KeyError, TypeError, ValueError):
         return None
 
 
@@ -226,125 +236,246 @@ def replica_throughput(world: int, units_per_replica: float, ms_per_step: float)
     return world * units_per_replica / (ms_per_step * 1e-3)
 
 
+class DeviceWorkload:
+    """One workload resident on the device: the seeded problem, `layers`
+    rotated copies of the cache and W_UV (more bytes than L2 holds), and the
+    output buffers of a step."""
+
+    def __init__(self, name: str, dev, layers: int = 0):
+        import torch
+        from mla_decode_attention_kv_gb300 import api
+        self.api = api
+        self.name = name
+        self.cfg = cfg = inputs.CONFIGS[name]
+        self.prob = prob = inputs.make_problem(cfg)
+        self.wm = work_model(prob)
+        self.dev = dev
+        self.dt = api.torch_dtype(cfg.dtype)
+        pdt = api.torch_dtype(cfg.part_dtype)
+
+        def t16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(self.dt)
+
+        self.q_abs, self.q_pe, W0 = t16(prob.q_abs), t16(prob.q_pe), t16(prob.W_UV)
+        cache0 = t16(prob.kv_cache)
+        self.kv_cur = t16(prob.kv_cur) if prob.kv_cur is not None else None
+        self.table = torch.from_numpy(prob.block_table).to(dev)
+        self.lens = torch.from_numpy(prob.seq_lens).to(dev)
+        self.per_layer = cache0.numel() * 2 + W0.numel() * 2
+        self.layers = layers or max(2, math.ceil(4 * L2_BYTES / self.per_layer))
+        self.caches = [cache0] + [cache0.clone() for _ in range(self.layers - 1)]
+        self.Ws = [W0] + [W0.clone() for _ in range(self.layers - 1)]
+        B, q, H, P = cfg.batch, cfg.q_len, cfg.heads, prob.num_parts
+        self.o_part = torch.empty((B, q, P, H, 512), dtype=pdt, device=dev)
+        self.lse_part = torch.empty((B, q, P, H), dtype=torch.float32, device=dev)
+        self.out = torch.empty((B * q, H * 128), dtype=self.dt, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(self, i, stream, ev=None):
+        li = i % self.layers
+        if ev is not None:
+            ev[0].record(stream)
+        self.api.mla_dcp_decode_partial(
+            self.q_abs, self.q_pe, self.caches[li], self.table, self.lens, self.cfg.num_shards,
+            kv_cur=self.kv_cur, scale=self.cfg.scale, o_part=self.o_part,
+            lse_part=self.lse_part, err_flag=self.err, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        self.api.mla_lse_combine_vup(self.o_part, self.lse_part, self.Ws[li], out=self.out,
+                                     err_flag=self.err, stream=stream)
+
+    def time_device(self, steps, warmup, stream, barrier):
+        """(ms of all `steps` steps, mean partial-kernel ms per step), device
+        time by CUDA events on the launching stream."""
+        import torch
+        for i in range(warmup):
+            self.step(i, stream)
+        barrier()
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        e0.record(stream)
+        for i in range(steps):
+            self.step(warmup + i, stream, kev[i])
+        e1.record(stream)
+        barrier()
+        total_ms = e0.elapsed_time(e1)
+        partial_ms = sum(a.elapsed_time(b) for a, b in kev) / steps
+        if self.err.item() != 0:
+            raise RuntimeError(f"{self.name}: device error {self.err.item()} in the timed region")
+        return total_ms, partial_ms
+
+    def time_e2e(self, steps, warmup, stream, barrier):
+        """ms of `steps` steps end to end through the public API: every step
+        copies its inputs from pinned host memory and its output back.  Two
+        sets of device input / output buffers alternate, and the copies run
+        on a second stream, so step i's copies overlap the kernels of its
+        neighbours (as a serving loop would run them).  One cudaMemcpyAsync
+        per direction and step; returns (ms, h2d bytes, d2h bytes)."""
+        import torch
+        prob, cfg, dev = self.prob, self.cfg, self.dev
+        parts = [("q_abs", prob.q_abs.view(np.int16)), ("q_pe", prob.q_pe.view(np.int16)),
+                 ("table", prob.block_table), ("lens", prob.seq_lens)]
+        if prob.kv_cur is not None:
+            parts.append(("kv_cur", prob.kv_cur.view(np.int16)))
+        offs, off = {}, 0
+        for name, a in parts:
+            offs[name] = off
+            off += (a.nbytes + 255) // 256 * 256
+        h_in = torch.empty(off, dtype=torch.uint8).pin_memory()
+        for name, a in parts:
+            h_in[offs[name]:offs[name] + a.nbytes].copy_(
+                torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).reshape(-1)))
+        d_in = [torch.empty(off, dtype=torch.uint8, device=dev) for _ in range(2)]
+        d_out = [torch.empty_like(self.out) for _ in range(2)]
+        h_out = [torch.empty(self.out.shape, dtype=torch.int16).pin_memory() for _ in range(2)]
+        likes = {"q_abs": self.q_abs, "q_pe": self.q_pe, "table": self.table, "lens": self.lens,
+                 "kv_cur": self.kv_cur}
+
+        def dview(k, name):
+            like = likes[name]
+            n = like.numel() * like.element_size()
+            return d_in[k][offs[name]:offs[name] + n].view(like.dtype).view(like.shape)
+
+        views = [{name: dview(k, name) for name, _ in parts} for k in range(2)]
+        copy = torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of buffer k landed
+        ev_used = [torch.cuda.Event() for _ in range(2)]    # kernels done with buffer k
+        ev_out = [torch.cuda.Event() for _ in range(2)]     # output k copied to the host
+        for k in range(2):
+            ev_used[k].record(stream)
+            ev_out[k].record(stream)
+
+        def e2e_step(i):
+            k, li = i % 2, i % self.layers
+            v = views[k]
+            with torch.cuda.stream(copy):
+                copy.wait_event(ev_used[k])
+                d_in[k].copy_(h_in, non_blocking=True)
+                ev_in[k].record(copy)
+            stream.wait_event(ev_in[k])
+            stream.wait_event(ev_out[k])
+            self.api.decode_step(v["q_abs"], v["q_pe"], self.caches[li], v["table"], v["lens"],
+                                 self.Ws[li], cfg.num_shards, kv_cur=v.get("kv_cur"),
+                                 scale=cfg.scale, o_part=self.o_part, lse_part=self.lse_part,
+                                 out=d_out[k], err_flag=self.err, stream=stream)
+            ev_used[k].record(stream)
+            with torch.cuda.stream(copy):
+                copy.wait_event(ev_used[k])
+                h_out[k].copy_(d_out[k].view(torch.int16), non_blocking=True)
+                ev_out[k].record(copy)
+
+        for i in range(warmup):
+            e2e_step(i)
+        barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        copy.wait_event(f0)
+        for i in range(steps):
+            e2e_step(warmup + i)
+        stream.wait_event(ev_out[0])
+        stream.wait_event(ev_out[1])
+        f1.record(stream)
+        barrier()
+        if self.err.item() != 0:
+            raise RuntimeError(f"{self.name}: device error {self.err.item()} in the e2e region")
+        return f0.elapsed_time(f1), off, self.wm["d2h_bytes"]
+
+    def roofline(self, partial_ms):
+        """Roofline of the partial kernel (+ its merge) from its own
+        CUDA-event time, against the measured peaks."""
+        wm = self.wm
+        peaks, peak_src = load_peaks()
+        part_s = partial_ms * 1e-3
+        hbm_ach = wm["partial_bytes"] / part_s / 1e9
+        tc_ach = wm["partial_flops"] / part_s / 1e12
+        hbm_frac = hbm_ach / peaks["hbm_gbs"]
+        tc_frac = tc_ach / peaks["bf16_tflops"]
+        if hbm_frac >= tc_frac:
+            roof = {"bound": "hbm", "achieved": round(hbm_ach, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(hbm_frac, 4)}
+        else:
+            roof = {"bound": "tensor", "achieved": round(tc_ach, 1), "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(tc_frac, 4)}
+        roof["traffic"] = traffic_from_profile(self.name)
+        roof["kernel"] = "mla_partial_kernel (+ mla_partial_merge_kernel)"
+        roof["kernel_ms"] = round(partial_ms, 5)
+        roof["alg_bytes_per_launch"] = wm["partial_bytes"]
+        roof["alg_flops_per_launch"] = wm["partial_flops"]
+        roof["tensor_frac"] = round(tc_frac, 4)
+        roof["hbm_frac"] = round(hbm_frac, 4)
+        roof["peak_source"] = ("measured (MEASURED_PEAKS.json, burst figures)"
+                               if peak_src == "measured" else "fallback")
+        return roof
+
+    def step_roofline(self, ms_per_step):
+        peaks, _ = load_peaks()
+        wm = self.wm
+        return max(wm["step_bytes"] / (peaks["hbm_gbs"] * 1e9),
+                   wm["step_flops"] / (peaks["bf16_tflops"] * 1e12)) / (ms_per_step * 1e-3)
+
+    def free(self):
+        for k in ("caches", "Ws", "o_part", "lse_part", "out", "q_abs", "q_pe", "kv_cur"):
+            setattr(self, k, None)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
-    from mla_decode_attention_kv_gb300 import api, build as mbuild
+    from mla_decode_attention_kv_gb300 import build as mbuild
     from mla_decode_attention_kv_gb300 import _ffi
 
     mbuild.build()
     _ffi.lib()
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
-    cfg = inputs.CONFIGS[args.config]
-    prob = inputs.make_problem(cfg)
-    wm = work_model(prob)
-    dt = api.torch_dtype(cfg.dtype)
-    pdt = api.torch_dtype(cfg.part_dtype)
-
-    def t16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt)
-
-    q_abs, q_pe, W0 = t16(prob.q_abs), t16(prob.q_pe), t16(prob.W_UV)
-    cache0 = t16(prob.kv_cache)
-    kv_cur = t16(prob.kv_cur) if prob.kv_cur is not None else None
-    table = torch.from_numpy(prob.block_table).to(dev)
-    lens = torch.from_numpy(prob.seq_lens).to(dev)
-    per_layer = cache0.numel() * 2 + W0.numel() * 2
-    layers = args.layers or max(2, math.ceil(4 * L2_BYTES / per_layer))
-    caches = [cache0] + [cache0.clone() for _ in range(layers - 1)]
-    Ws = [W0] + [W0.clone() for _ in range(layers - 1)]
-    B, q, H, P = cfg.batch, cfg.q_len, cfg.heads, prob.num_parts
-    o_part = torch.empty((B, q, P, H, 512), dtype=pdt, device=dev)
-    lse_part = torch.empty((B, q, P, H), dtype=torch.float32, device=dev)
-    out = torch.empty((B * q, H * 128), dtype=dt, device=dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
-
-    def step(i, ev=None):
-        li = i % layers
-        if ev is not None:
-            ev[0].record(stream)
-        api.mla_dcp_decode_partial(q_abs, q_pe, caches[li], table, lens, cfg.num_shards,
-                                   kv_cur=kv_cur, scale=cfg.scale, o_part=o_part,
-                                   lse_part=lse_part, err_flag=err, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        api.mla_lse_combine_vup(o_part, lse_part, Ws[li], out=out, err_flag=err, stream=stream)
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
 
+    wl = DeviceWorkload(args.config, dev, args.layers)
     sampler = ClockSampler(local_rank) if rank == 0 else None
-    for i in range(args.warmup):
-        step(i)
-    barrier()
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
     w0 = time.time()
-    e0.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i, kev[i])
-    e1.record(stream)
-    barrier()
+    total_ms, partial_ms = wl.time_device(args.steps, args.warmup, stream, barrier)
     w1 = time.time()
-    total_ms = e0.elapsed_time(e1)
-    partial_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
-    if err.item() != 0:
-        raise RuntimeError(f"device error {err.item()} during the timed region")
-
-    # ---- end to end through the public API with pinned host buffers.  The
-    # step's inputs are staged in one pinned buffer (each at a 256-byte
-    # aligned offset) and moved with one copy; the calls get device views.
-    parts = [("q_abs", prob.q_abs.view(np.int16)), ("q_pe", prob.q_pe.view(np.int16)),
-             ("table", prob.block_table), ("lens", prob.seq_lens)]
-    if prob.kv_cur is not None:
-        parts.append(("kv_cur", prob.kv_cur.view(np.int16)))
-    offs, off = {}, 0
-    for name, a in parts:
-        offs[name] = off
-        off += (a.nbytes + 255) // 256 * 256
-    h_in = torch.empty(off, dtype=torch.uint8).pin_memory()
-    for name, a in parts:
-        h_in[offs[name]:offs[name] + a.nbytes].copy_(
-            torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).reshape(-1)))
-    d_in = torch.empty(off, dtype=torch.uint8, device=dev)
-    wm["h2d_bytes"] = off   # what is copied: the inputs and their alignment padding
-
-    def dview(name, like):
-        n = like.numel() * like.element_size()
-        return d_in[offs[name]:offs[name] + n].view(like.dtype).view(like.shape)
-
-    d_qa, d_qp = dview("q_abs", q_abs), dview("q_pe", q_pe)
-    d_tab, d_len = dview("table", table), dview("lens", lens)
-    d_cur = dview("kv_cur", kv_cur) if kv_cur is not None else None
-    h_out = torch.empty((B * q, H * 128), dtype=torch.int16).pin_memory()
-
-    def e2e_step(i):
-        li = i % layers
-        d_in.copy_(h_in, non_blocking=True)
-        api.decode_step(d_qa, d_qp, caches[li], d_tab, d_len, Ws[li], cfg.num_shards,
-                        kv_cur=d_cur, scale=cfg.scale, o_part=o_part, lse_part=lse_part,
-                        out=out, err_flag=err, stream=stream)
-        h_out.copy_(out.view(torch.int16), non_blocking=True)
-
-    for i in range(args.warmup):
-        e2e_step(i)
-    barrier()
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for i in range(args.steps):
-        e2e_step(args.warmup + i)
-    f1.record(stream)
-    barrier()
-    e2e_ms = f0.elapsed_time(f1)
+    e2e_ms, h2d_bytes, d2h_bytes = wl.time_e2e(args.steps, args.warmup, stream, barrier)
     clocks = ClockSampler.summarize(sampler.stop(), w0, w1) if sampler else None
-
     total_ms, e2e_ms, partial_ms = max_over_ranks([total_ms, e2e_ms, partial_ms], world, dev)
+
+    extras = {}
+    names = [] if args.extra == "none" else [n for n in args.extra.split(",") if n]
+    prob_for_cpu = wl.prob
+    wm = wl.wm
+    line_roof = wl.roofline(partial_ms)
+    step_roof = wl.step_roofline(total_ms / args.steps)
+    layers, per_layer = wl.layers, wl.per_layer
+    wl.free()
+    del wl
+    torch.cuda.empty_cache()
+    for name in names:
+        if name == args.config:
+            continue
+        x = DeviceWorkload(name, dev)
+        steps = max(20, min(args.steps, 200))
+        t_ms, p_ms = x.time_device(steps, max(3, args.warmup), stream, barrier)
+        t_ms, p_ms = max_over_ranks([t_ms, p_ms], world, dev)
+        ms = t_ms / steps
+        extras[name] = {
+            "workload": WORKLOAD_TEXT[name],
+            "value": round(replica_throughput(world, x.wm["kv_bytes"], ms) / 1e12, 4),
+            "unit": "TB/s",
+            "tokens_per_s": round(replica_throughput(world, x.wm["query_tokens"], ms), 1),
+            "ms_per_step": round(ms, 5), "steps": steps,
+            "step_roofline_frac": round(x.step_roofline(ms), 4),
+            "roofline": x.roofline(p_ms),
+        }
+        x.free()
+        del x
+        torch.cuda.empty_cache()
     if rank != 0:
         return None
 
@@ -352,30 +483,6 @@ def run_ours(args, rank, world, local_rank):
     kv_tbs = replica_throughput(world, wm["kv_bytes"], ms_per_step) / 1e12
     tok_s = replica_throughput(world, wm["query_tokens"], ms_per_step)
     e2e_tbs = replica_throughput(world, wm["kv_bytes"], e2e_ms / args.steps) / 1e12
-    peaks, peak_src = load_peaks()
-    part_s = partial_ms * 1e-3
-    hbm_ach = wm["partial_bytes"] / part_s / 1e9
-    tc_ach = wm["partial_flops"] / part_s / 1e12
-    hbm_frac = hbm_ach / peaks["hbm_gbs"]
-    tc_frac = tc_ach / peaks["bf16_tflops"]
-    if hbm_frac >= tc_frac:
-        roof = {"bound": "hbm", "achieved": round(hbm_ach, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(hbm_frac, 4)}
-    else:
-        roof = {"bound": "tensor", "achieved": round(tc_ach, 1), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(tc_frac, 4)}
-    roof["traffic"] = traffic_from_profile(args.config)
-    roof["kernel"] = "mla_partial_kernel (+ mla_partial_merge_kernel)"
-    roof["kernel_ms"] = round(partial_ms, 5)
-    roof["alg_bytes_per_launch"] = wm["partial_bytes"]
-    roof["alg_flops_per_launch"] = wm["partial_flops"]
-    roof["tensor_frac"] = round(tc_frac, 4)
-    roof["hbm_frac"] = round(hbm_frac, 4)
-    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" \
-        else "fallback"
-    step_s = ms_per_step * 1e-3
-    step_roof = max(wm["step_bytes"] / (peaks["hbm_gbs"] * 1e9),
-                    wm["step_flops"] / (peaks["bf16_tflops"] * 1e12)) / step_s
     line = {
         "metric": METRIC,
         "value": round(kv_tbs, 4),
@@ -389,7 +496,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": cfg.dtype,
+        "dtype": inputs.CONFIGS[args.config].dtype,
         "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config,
                    "query_tokens_per_step": wm["query_tokens"],
@@ -397,15 +504,19 @@ def run_ours(args, rank, world, local_rank):
                    "l2": f"inputs larger than L2: {layers} rotated layer caches + W_UV "
                          f"({layers * per_layer / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": roof,
+        "roofline": line_roof,
         "e2e": {"value": round(e2e_tbs, 4), "unit": "TB/s",
-                "h2d_bytes_per_step": wm["h2d_bytes"], "d2h_bytes_per_step": wm["d2h_bytes"]},
-        # per step: partial kernel, its split-shard merge kernel, fused combine + V-up
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+                "copies": "double-buffered inputs/outputs, copies on a second stream"},
+        # per step: partial kernel, its split-shard merge kernel, fused combine + V-up;
+        # the same three per step in the e2e leg (which also runs the copies)
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
+    if extras:
+        line["extra_workloads"] = extras
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(prob, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(prob_for_cpu, args.cpu_seconds)
     return line
 
 
@@ -502,10 +613,12 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=sorted(inputs.CONFIGS), default="dsv3")
+    ap.add_argument("--config", choices=sorted(inputs.CONFIGS), default="verylong")
+    ap.add_argument("--extra", default="dsv3,mtp,ragged",
+                    help="other workloads timed device-only (comma list, or none)")
     ap.add_argument("--layers", type=int, default=0, help="layer caches rotated (0 = auto)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="budget of the CPU-oracle baseline sample")

@@ -29,7 +29,8 @@
  *     see (null pointer, bad size, bad dtype, misalignment, launch failure).
  *     Nothing is launched when a host check fails.
  *   - Errors only the device can see (a block_table entry outside
- *     [0, num_blocks), a pipeline wait that ran out of its spin budget) are
+ *     [0, num_blocks), a seq_lens entry outside [0, max_blocks*block_size],
+ *     a pipeline wait that ran out of its spin budget) are
  *     written to *err_flag (a caller-owned device int32, may be NULL) with
  *     the first writer winning; read it after synchronising.  When it is
  *     non-zero the outputs of that call are unspecified.  No kernel traps or
@@ -63,7 +64,12 @@ typedef enum {
 } mla_status;
 
 /* Device error codes written to *err_flag. */
-enum { MLA_DEV_OK = 0, MLA_DEV_BAD_BLOCK_ID = 1, MLA_DEV_WAIT_TIMEOUT = 2 };
+enum {
+  MLA_DEV_OK = 0,
+  MLA_DEV_BAD_BLOCK_ID = 1,  /* a block_table entry outside [0, num_blocks)       */
+  MLA_DEV_WAIT_TIMEOUT = 2,  /* a pipeline wait ran out of its spin budget         */
+  MLA_DEV_BAD_SEQ_LEN = 3    /* a seq_lens entry outside [0, max_blocks*block_size] */
+};
 
 enum {
   MLA_D_LATENT = 512, /* kv_lora_rank: width of c_KV  ([TP] "物理矛盾")          */
@@ -102,7 +108,8 @@ enum {
  *   kv_cache   [num_blocks, block_size, 576] in_dtype
  *   block_table[B, max_blocks] int32   physical block ids; entries past
  *              ceil(L_b / block_size) are never read
- *   seq_lens   [B] int32 (device)  history lengths, 0 <= L_b <= max_blocks*block_size
+ *   seq_lens   [B] int32 (device)  history lengths, 0 <= L_b <= max_blocks*block_size;
+ *              an entry outside that range sets MLA_DEV_BAD_SEQ_LEN
  *   kv_cur     [B, q_len, 576] in_dtype, or NULL (no CURRENT segment)
  *   B >= 1; 1 <= q_len <= 8; 1 <= H <= 128; block_size in {16,32,64,128,256};
  *   1 <= num_shards <= 64; scale > 0 (1/sqrt(192) for the 128+64 head width)
@@ -133,33 +140,39 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
 
 /*
  * mla_dcp_decode_partial_workspace_size -- bytes of workspace that
- * mla_dcp_decode_partial needs on the current device for these sizes (about
- * 0.5 MiB per resident CTA pair, plus 4 bytes per (b, i, part)).  Returns 0 if
- * the sizes are invalid or the device cannot run the kernel.  A library
- * addition with no counterpart in the sources.
+ * mla_dcp_decode_partial needs on the current device: about 0.5 MiB per
+ * CTA pair the device keeps resident (FP32 partials need twice that), with
+ * no term that grows with B, q_len or num_shards.  The sizes are only
+ * validated: it returns 0 if they are invalid or the device cannot run the
+ * kernel.  A library addition with no counterpart in the sources.
  */
 uint64_t mla_dcp_decode_partial_workspace_size(int B, int q_len, int num_shards, int has_current);
 
 /*
  * mla_dcp_decode_partial_noalloc -- mla_dcp_decode_partial with no
  * workspace argument and no allocation of any kind.  A library addition
- * with no counterpart in the sources.
+ * with no counterpart in the sources.  It is for callers that cannot hand
+ * the library device memory: for example a serving runtime whose memory
+ * planner gives all free device memory to its own pool at start-up, so that
+ * no buffer can be allocated or lent for a single call.
  *
- * Same arguments, results and errors as mla_dcp_decode_partial, whose
- * split-shard workspace it takes from a fixed 24 MiB device array inside the
- * library.  That holds the workspace of up to 95 CTA pairs with BF16 / FP16
- * partials, or 47 with FP32 partials; when this device needs more (e.g. FP32
- * partials on a GPU with more than 47 resident pairs) the call returns
- * MLA_ERR_BAD_SHAPE and launches nothing.
+ * Same arguments, results and errors as mla_dcp_decode_partial (its
+ * argument checks run first, in the same order), whose split-shard
+ * workspace it takes from a fixed 24 MiB device array inside the library.
+ * That holds the workspace of up to 95 CTA pairs with BF16 / FP16 partials,
+ * or 47 with FP32 partials.  When this device needs more (FP32 partials on
+ * a GPU with more than 47 resident pairs, such as GB300's 76) the call runs
+ * as mla_dcp_decode_partial with workspace NULL: every pair takes whole
+ * shards and no scratch is used.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) and the kernel's occupancy; make that first call
- *     outside any stream capture.  Later calls only launch kernels, so they
- *     can be captured into a CUDA graph.
+ *     outside any stream capture.  The address is looked up again if the
+ *     device's context changed (after cudaDeviceReset).
  *   - Nothing in the array has to start at zero: every call rewrites each
  *     record it reads.
  *   - All calls on a device share the array: calls that may overlap in time
- *     (different streams, or graphs replayed concurrently) race on it and
- *     must be serialised by the caller.
+ *     (on different streams, say) race on it and must be serialised by the
+ *     caller.
  */
 int mla_dcp_decode_partial_noalloc(const void* q_abs, const void* q_pe, const void* kv_cache,
                                    const int32_t* block_table, const int32_t* seq_lens,

@@ -46,21 +46,26 @@ def _need(t: torch.Tensor, name: str):
 _WORKSPACES = {}
 
 
-def partial_workspace(device, B: int, q_len: int, num_shards: int, has_current: bool):
-    """The default workspace of mla_dcp_decode_partial on `device` (one per
-    device, grown as needed), or None for sizes the library rejects.  Calls
-    that may run at the same time on different streams need workspaces of
-    their own."""
+def partial_workspace(device, B: int, q_len: int, num_shards: int, has_current: bool,
+                      stream=None):
+    """The default workspace of mla_dcp_decode_partial on `device` for calls on
+    `stream` (one per (device, stream), grown as needed), or None for sizes
+    the library rejects.  Calls on one stream run one after another, so they
+    can share it; calls on different streams get different workspaces.  Two
+    calls that may overlap in time on the same stream handle (graphs replayed
+    concurrently, say) must pass workspaces of their own."""
     device = torch.device(device)
     with torch.cuda.device(device):
         need = int(_ffi.lib().mla_dcp_decode_partial_workspace_size(
             B, q_len, num_shards, 1 if has_current else 0))
+        s = stream if stream is not None else torch.cuda.current_stream()
     if need == 0:
         return None      # invalid sizes: the call itself reports them
-    ws = _WORKSPACES.get(device.index)
+    key = (device.index, s.cuda_stream)
+    ws = _WORKSPACES.get(key)
     if ws is None or ws.numel() < need:
         ws = torch.empty(need, dtype=torch.uint8, device=device)
-        _WORKSPACES[device.index] = ws
+        _WORKSPACES[key] = ws
     return ws
 
 
@@ -74,9 +79,10 @@ def mla_dcp_decode_partial(q_abs, q_pe, kv_cache, block_table, seq_lens, num_sha
     block_table [B, max_blocks] int32, seq_lens [B] int32 (history lengths),
     kv_cur [B, q, 576] or None.  Returns o_part [B, q, P, H, 512] and
     lse_part [B, q, P, H] (float32), P = num_shards + (kv_cur is not None).
-    workspace: "default" (the device's shared one), a uint8 CUDA tensor of at
-    least mla_dcp_decode_partial_workspace_size bytes, or None (pairs of CTAs
-    then take whole shards)."""
+    workspace: "default" (one kept per device and stream, see
+    partial_workspace), a uint8 CUDA tensor of at least
+    mla_dcp_decode_partial_workspace_size bytes, or None (pairs of CTAs then
+    take whole shards)."""
     B, q_len, H, _ = q_abs.shape
     num_blocks, bs, _ = kv_cache.shape
     P = num_shards + (1 if kv_cur is not None else 0)
@@ -91,7 +97,8 @@ def mla_dcp_decode_partial(q_abs, q_pe, kv_cache, block_table, seq_lens, num_sha
     if isinstance(workspace, str):
         if workspace != "default":
             raise ValueError("workspace must be 'default', a tensor or None")
-        workspace = partial_workspace(q_abs.device, B, q_len, num_shards, kv_cur is not None)
+        workspace = partial_workspace(q_abs.device, B, q_len, num_shards, kv_cur is not None,
+                                      stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = _ffi.lib().mla_dcp_decode_partial(
         _p(q_abs), _p(q_pe), _p(kv_cache), _p(block_table), _p(seq_lens), _p(kv_cur),
@@ -106,8 +113,9 @@ def mla_dcp_decode_partial_noalloc(q_abs, q_pe, kv_cache, block_table, seq_lens,
                                    num_shards: int, *, o_part, lse_part, kv_cur=None,
                                    scale: float = DEFAULT_SCALE, err_flag=None, stream=None):
     """mla_dcp_decode_partial with the library's fixed scratch array instead of
-    a workspace: allocates nothing (o_part / lse_part are required).  Calls
-    that may overlap in time share that array and must be serialised."""
+    a workspace: allocates nothing (o_part / lse_part are required), for
+    callers that cannot lend the library device memory.  Calls that may
+    overlap in time share that array and must be serialised."""
     B, q_len, H, _ = q_abs.shape
     num_blocks, bs, _ = kv_cache.shape
     for t, n in ((q_abs, "q_abs"), (q_pe, "q_pe"), (kv_cache, "kv_cache"),

@@ -95,17 +95,20 @@ const char* mla_device_error_string(int code) {
     case MLA_DEV_OK: return "ok";
     case MLA_DEV_BAD_BLOCK_ID: return "block_table entry outside [0, num_blocks)";
     case MLA_DEV_WAIT_TIMEOUT: return "a pipeline wait exceeded its spin budget";
+    case MLA_DEV_BAD_SEQ_LEN: return "seq_lens entry outside [0, max_blocks * block_size]";
     default: return "unknown device error";
   }
 }
 
-int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_cache,
-                           const int32_t* block_table, const int32_t* seq_lens,
-                           const void* kv_cur, int B, int q_len, int H, int num_blocks,
-                           int block_size, int max_blocks, int num_shards, float scale,
-                           int in_dtype, int part_dtype, void* o_part, float* lse_part,
-                           int32_t* err_flag, void* workspace, uint64_t workspace_bytes,
-                           mla_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// Host checks of mla_dcp_decode_partial's arguments (all but the workspace).
+int check_partial_args(const void* q_abs, const void* q_pe, const void* kv_cache,
+                       const int32_t* block_table, const int32_t* seq_lens, const void* kv_cur,
+                       int B, int q_len, int H, int num_blocks, int block_size, int max_blocks,
+                       int num_shards, float scale, int in_dtype, int part_dtype,
+                       const void* o_part, const float* lse_part) {
   if (!q_abs || !q_pe || !kv_cache || !block_table || !seq_lens || !o_part || !lse_part)
     return MLA_ERR_NULL_POINTER;
   if (!is_half_dtype(in_dtype) || !is_part_dtype(part_dtype)) return MLA_ERR_BAD_DTYPE;
@@ -120,9 +123,28 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
       static_cast<int64_t>(B) * q_len * H > INT32_MAX / 2)
     return MLA_ERR_BAD_SHAPE;
   if (!aligned16(q_abs) || !aligned16(q_pe) || !aligned16(kv_cache) || !aligned16(o_part) ||
-      (kv_cur && !aligned16(kv_cur)) || !aligned16(lse_part) ||
-      (workspace && reinterpret_cast<uintptr_t>(workspace) % 256 != 0))
+      (kv_cur && !aligned16(kv_cur)) || !aligned16(lse_part))
     return MLA_ERR_MISALIGNED;
+  if (static_cast<int64_t>(B) * q_len * (num_shards + (kv_cur ? 1 : 0)) > INT32_MAX)
+    return MLA_ERR_BAD_SHAPE;
+  return MLA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_cache,
+                           const int32_t* block_table, const int32_t* seq_lens,
+                           const void* kv_cur, int B, int q_len, int H, int num_blocks,
+                           int block_size, int max_blocks, int num_shards, float scale,
+                           int in_dtype, int part_dtype, void* o_part, float* lse_part,
+                           int32_t* err_flag, void* workspace, uint64_t workspace_bytes,
+                           mla_stream_t stream) {
+  const int rc = check_partial_args(q_abs, q_pe, kv_cache, block_table, seq_lens, kv_cur, B,
+                                    q_len, H, num_blocks, block_size, max_blocks, num_shards,
+                                    scale, in_dtype, part_dtype, o_part, lse_part);
+  if (rc != MLA_OK) return rc;
+  if (workspace && reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return MLA_ERR_MISALIGNED;
 
   const bool bf16 = in_dtype == MLA_BF16;
   const int box_k = block_size < mla::kPartialBoxK ? block_size : mla::kPartialBoxK;
@@ -146,6 +168,7 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
   }
 
   mla::PartialParams pp;
+  pp.kv_base = static_cast<const uint8_t*>(kv_cache);
   pp.block_table = block_table;
   pp.seq_lens = seq_lens;
   pp.o_part = o_part;
@@ -160,9 +183,7 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
   pp.S = num_shards;
   pp.has_cur = kv_cur ? 1 : 0;
   pp.P = num_shards + pp.has_cur;
-  const int64_t units = static_cast<int64_t>(B) * q_len * pp.P;
-  if (units > INT32_MAX) return MLA_ERR_BAD_SHAPE;
-  pp.num_units = static_cast<int>(units);
+  pp.num_units = B * q_len * pp.P;   // checked above to fit an int
   pp.box_rows = box_k;
   pp.box_rows_v = box_v;
   pp.scale_log2 = scale * 1.4426950408889634f;
@@ -204,16 +225,45 @@ constexpr size_t kNoAllocScratchBytes = size_t{24} << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
-// Device address of g_noalloc_scratch, looked up once per device.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current, and again if the device's context changed since (after a
+// cudaDeviceReset the array lives in a new context, at a new address).
 void* noalloc_scratch() {
   static void* addr[64] = {nullptr};
+  static CUcontext owner[64] = {nullptr};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (!get_ctx) return nullptr;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return nullptr;   // null before the first runtime call
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev] && cudaGetSymbolAddress(&addr[dev], g_noalloc_scratch) != cudaSuccess) {
-    cudaGetLastError();
-    addr[dev] = nullptr;
+  if (!ctx || !addr[dev] || owner[dev] != ctx) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess) {   // sets up the context
+      cudaGetLastError();
+      return nullptr;
+    }
+    if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return nullptr;
+    addr[dev] = a;
+    owner[dev] = ctx;
   }
   return addr[dev];
 }
@@ -225,16 +275,26 @@ int mla_dcp_decode_partial_noalloc(const void* q_abs, const void* q_pe, const vo
                                    int block_size, int max_blocks, int num_shards, float scale,
                                    int in_dtype, int part_dtype, void* o_part, float* lse_part,
                                    int32_t* err_flag, mla_stream_t stream) {
-  if (!is_part_dtype(part_dtype)) return MLA_ERR_BAD_DTYPE;
+  // the same argument checks, in the same order, as the workspace entry point
+  const int rc = check_partial_args(q_abs, q_pe, kv_cache, block_table, seq_lens, kv_cur, B,
+                                    q_len, H, num_blocks, block_size, max_blocks, num_shards,
+                                    scale, in_dtype, part_dtype, o_part, lse_part);
+  if (rc != MLA_OK) return rc;
   const int clusters = mla::partial_max_clusters();
   if (clusters < 1) return MLA_ERR_CUDA;
   const size_t need = mla::partial_workspace_bytes(clusters, part_dtype == MLA_FP32 ? 4 : 2);
-  if (need > kNoAllocScratchBytes) return MLA_ERR_BAD_SHAPE;
-  void* scratch = noalloc_scratch();
-  if (!scratch) return MLA_ERR_CUDA;
+  void* scratch = nullptr;
+  if (need <= kNoAllocScratchBytes) {
+    scratch = noalloc_scratch();
+    if (!scratch) return MLA_ERR_CUDA;
+  }
+  // when the split-shard scratch of this device's pairs does not fit the
+  // array (fp32 partials on a GPU with more than 47 pairs), every pair takes
+  // whole shards instead: the same results, with no scratch at all
   return mla_dcp_decode_partial(q_abs, q_pe, kv_cache, block_table, seq_lens, kv_cur, B, q_len, H,
                                 num_blocks, block_size, max_blocks, num_shards, scale, in_dtype,
-                                part_dtype, o_part, lse_part, err_flag, scratch, need, stream);
+                                part_dtype, o_part, lse_part, err_flag, scratch,
+                                scratch ? need : 0, stream);
 }
 
 int mla_lse_combine(const void* o_part, const float* lse_part, int num_parts, const void* o_local,

@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(256) mla_gather_kernel(const uint4* kv_cache,
   constexpr int kUnits = 576 * 2 / 16;
   uint4* out = dst + (static_cast<int64_t>(b) * max_len + t) * kUnits;
   const int L = seq_lens[b];
+  if ((L < 0 || L > max_blocks * bs) && t == 0 && lane == 0) set_error(err, kDevBadSeqLen);
   bool valid = t < L && t < max_blocks * bs;
   int64_t src_row = 0;
   if (valid) {

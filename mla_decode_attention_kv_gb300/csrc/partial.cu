@@ -43,6 +43,7 @@
 // Every wait is bounded; on timeout the kernel records MLA_DEV_WAIT_TIMEOUT,
 // raises an abort flag, drains its own copies and MMAs, frees TMEM, returns.
 #include <climits>
+#include <mutex>
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -73,7 +74,13 @@ __device__ __forceinline__ UnitInfo unit_info(const PartialParams& pp, int u) {
     ui.hi = ui.i + 1;
   } else {
     int L = pp.seq_lens[ui.b];
-    L = max(0, min(L, pp.max_blocks * pp.bs));
+    const int cap = pp.max_blocks * pp.bs;
+    if (L < 0 || L > cap) {
+      // a history longer than its block-table row (or negative): flagged,
+      // then clamped so that no access leaves the table
+      set_error(pp.err, kDevBadSeqLen);
+      L = max(0, min(L, cap));
+    }
     const int chunk = pp.S * pp.bs;
     const int len = L > 0 ? pp.bs * ((L + chunk - 1) / chunk) : 0;
     ui.lo = min(L, ui.p * len);
@@ -208,9 +215,12 @@ enum : int {
   B_MMA_DONE_B = B_O_FIXED + 1,
   B_COUNT = B_MMA_DONE_B + 1
 };
-// barriers + TMEM slot + abort flag + 4 warp flags + 8 Q-chunk counters must
-// fit the barrier block
-static_assert((B_COUNT + 4) * 8 + 32 <= 512, "barrier block");
+// barriers + TMEM slot + abort flag + 4 warp flags + 8 Q-chunk counters +
+// the producer's tile count must fit the barrier block
+static_assert((B_COUNT + 9) * 8 <= 512, "barrier block");
+
+// Tiles the QK CTA's L2 prefetch runs ahead of its TMA producer.
+constexpr int kPrefetchAhead = 2;
 
 template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
@@ -235,6 +245,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + B_COUNT + 1);
   volatile uint32_t* warp_flags = reinterpret_cast<volatile uint32_t*>(bar + B_COUNT + 2);
   int* q_readers = reinterpret_cast<int*>(bar + B_COUNT + 4);   // warps done with Q chunk c
+  volatile int* k_progress = reinterpret_cast<volatile int*>(bar + B_COUNT + 8);   // tiles issued
 
   const uint32_t rank = cluster_ctarank();
   const int warp = threadIdx.x >> 5;
@@ -275,6 +286,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       mbar_arrive_expect_tx(&bar[B_P_FULL + 1], L::kMsgBytes);
     }
     *abort_flag = 0;
+    *k_progress = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -471,6 +483,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       it.start(pp, rng);
       int cs = 0;
       int qloads = 0;
+      int ntile = 0;
       bool ok = true;
       const int nbox = TILE / br_k;      // boxes per chunk of a tile (1, 2 or 8)
       const bool boxlane = lane < nbox;
@@ -522,6 +535,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           ++cs;
         }
         if (!ok) break;
+        if (lane == 0) *k_progress = ++ntile;   // paces the L2 prefetch warp
         id_cur = id_next;
         it = nx;
       }
@@ -587,6 +601,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         if (ui.ntiles != 0) continue;
         const int64_t row0 = (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H;
         for (int h = t; h < pp.H; h += 64) pp.lse_part[row0 + h] = -INFINITY;
+      }
+      if (warp == 2) {
+        // ---------------------------------------------- rank 0: L2 prefetch
+        // Walks the pair's tiles kPrefetchAhead ahead of the TMA producer and
+        // asks L2 for each box's rows (one contiguous run of a page), so the
+        // ring's loads find their data in L2: the ring then only has to
+        // cover L2 latency, not HBM latency.  Lane l takes box l, as the
+        // producer does; a box never crosses a page.  Prefetch is a hint:
+        // bad block ids are left for the producer to report, and the warp
+        // stops (without an error) if it ever waits too long.
+        TileIter<TILE> pf;
+        pf.start(pp, rng);
+        const int nbox = TILE / br_k;
+        int g = 0;
+        while (pf.valid) {
+          bool go = true;
+          for (uint32_t spin = 0; g - *k_progress > kPrefetchAhead; ++spin) {
+            if (spin >= kSpinLimit || *abort_flag) {
+              go = false;
+              break;
+            }
+            __nanosleep(128);
+          }
+          if (!go) break;
+          if (lane < nbox && !pf.ui.current) {
+            const int tk = pf.ui.lo + pf.j * TILE + lane * br_k;
+            if (tk < pf.ui.hi) {
+              const int id = __ldg(pp.block_table + static_cast<int64_t>(pf.ui.b) * pp.max_blocks +
+                                   (tk >> bs_shift));
+              if (id >= 0 && id < pp.num_blocks) {
+                const int64_t row = (static_cast<int64_t>(id) << bs_shift) + (tk & (pp.bs - 1));
+                const int rows = min(br_k, pf.ui.hi - tk);
+                prefetch_l2(pp.kv_base + row * 1152, static_cast<uint32_t>(rows) * 1152u);
+              }
+            }
+          }
+          pf.advance(pp);
+          ++g;
+        }
       }
     } else {
       // ------------------------------------------------ rank 0: softmax
@@ -1089,11 +1142,17 @@ __global__ void __launch_bounds__(256) mla_partial_merge_kernel(PartialParams pp
 // ---------------------------------------------------------------- launcher
 // Sets the kernel's shared-memory limit and finds how many CTA pairs fit on
 // the current device at once (cached per device).
+// The cache is keyed by device ordinal and guarded by a lock, so host threads
+// that make their first call at the same time set it up once.  A device reset
+// (cudaDeviceReset) does not clear it; the occupancy it holds stays valid for
+// the same GPU.
 template <bool BF16>
 static int prepare_partial(int* clusters) {
   static int cache[64] = {0};
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  std::lock_guard<std::mutex> lock(mu);
   if (cache[dev] == 0) {
     auto kern = mla_partial_kernel<BF16>;
     constexpr int smem = PairSmem::kTotal;

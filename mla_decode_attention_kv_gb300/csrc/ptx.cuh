@@ -24,6 +24,7 @@ enum DeviceError : int {
   kDevOk = 0,
   kDevBadBlockId = 1,     // block_table entry outside [0, num_blocks)
   kDevWaitTimeout = 2,    // a pipeline wait exceeded its spin budget
+  kDevBadSeqLen = 3,      // seq_lens entry outside [0, max_blocks * block_size]
 };
 
 __device__ __forceinline__ void set_error(int* err, int code) {
@@ -181,6 +182,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
       : "memory");
+}
+
+// Fetch `bytes` (multiple of 16) of global memory at p (16-byte aligned) into
+// L2 without waiting: a hint that loads TMA will issue later hit in L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -38,6 +38,7 @@ def test_error_strings(lib):
     for code in range(1, 8):
         assert lib.mla_get_error_string(code) != b"unknown status"
     assert lib.mla_device_error_string(1).startswith(b"block_table")
+    assert lib.mla_device_error_string(3).startswith(b"seq_lens")
     assert lib.mla_version() >= 100
 
 

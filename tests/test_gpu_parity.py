@@ -223,17 +223,29 @@ def test_extreme_tile_late_in_shard():
     dp = DeviceProblem(prob)
     o_part, lse_part = dp.partial(part_dtype=torch.float32)
     torch.cuda.synchronize()
+    assert dp.err.item() == 0
     _check_partials(dp, o_part, lse_part)
 
 
 def test_equal_logit_rows():
+    """A sequence whose query is all zero: every logit is 0, so each part's
+    LSE is ln(tokens) and the combined LSE is ln(L).  Checked on every shard
+    partial, the combined LSE and the output."""
     cfg = inputs.DecodeConfig(name="eq", batch=3, heads=128, q_len=1, num_shards=4,
                               block_size=32, ragged=(40, 500), dtype="fp16",
                               part_dtype="fp16", equal_logit_rows=(1,), seed=81)
     dp = DeviceProblem(inputs.make_problem(cfg))
-    out = dp.step()
+    o_part, lse_part = dp.partial()
+    lse = torch.empty((cfg.batch, cfg.heads), dtype=torch.float32, device=dp.dev)
+    out = api.mla_lse_combine_vup(o_part, lse_part, dp.W, lse_out=lse, err_flag=dp.err)
     torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    _check_partials(dp, o_part, lse_part)
     _, ref_l, ref_out = om.decode_reference(dp.prob)
+    assert_lse_close(f64(lse).reshape(ref_l.shape), ref_l, "lse")
+    # the closed form of the all-equal row, independent of the oracle
+    L = int(dp.prob.seq_lens[1])
+    assert np.abs(f64(lse)[1] - np.log(L)).max() <= 2e-3
     assert_out_close(f64(out), ref_out, "out")
 
 
@@ -381,6 +393,31 @@ def test_bad_block_id_sets_device_error():
     dp2.partial()
     torch.cuda.synchronize()
     assert dp2.err.item() == 0
+
+
+@pytest.mark.parametrize("bad", [-1, "over"])
+def test_bad_seq_len_sets_device_error(bad):
+    """A history length outside [0, max_blocks * block_size] (a corrupt
+    length, set on the host) is reported through the device error word by
+    the partial kernel and by the gather; the context stays usable."""
+    cfg = inputs.DecodeConfig(name="bl", batch=3, heads=128, q_len=1, num_shards=2,
+                              block_size=32, history=100, seed=92)
+    prob = inputs.make_problem(cfg)
+    cap = prob.max_blocks * cfg.block_size
+    prob.seq_lens[1] = cap + 1 if bad == "over" else bad
+    dp = DeviceProblem(prob)
+    dp.partial()
+    torch.cuda.synchronize()
+    assert dp.err.item() == 3
+    dp.err.zero_()
+    api.mla_gather_kv(dp.cache, dp.table, dp.lens, 128, err_flag=dp.err)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 3
+    dp2 = DeviceProblem(inputs.make_problem(cfg))
+    o_part, lse_part = dp2.partial()
+    torch.cuda.synchronize()
+    assert dp2.err.item() == 0
+    _check_partials(dp2, o_part, lse_part)
 
 
 def test_host_errors_launch_nothing():

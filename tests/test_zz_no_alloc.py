@@ -47,21 +47,38 @@ def test_noalloc_matches_workspace_entry_point_twice(name):
         assert torch.equal(o, ref_o) and torch.equal(l, ref_l)
 
 
-def test_noalloc_rejects_what_the_array_cannot_hold():
-    """FP32 partials need twice the scratch of 16-bit ones; the call is
-    refused (MLA_ERR_BAD_SHAPE) exactly when that exceeds the 24 MiB array."""
+def test_noalloc_fp32_partials():
+    """FP32 partials need twice the scratch of 16-bit ones.  When that exceeds
+    the 24 MiB array (a GPU with more than 47 resident CTA pairs) the call
+    takes whole shards with no scratch, so it matches the workspace-free
+    entry point; otherwise the workspace one.  Two calls in a row."""
     dp = DeviceProblem(inputs.make_problem(CASES["split"]))
     need_fp32 = api._ffi.lib().mla_dcp_decode_partial_workspace_size(1, 1, 1, 0)
-    o, l = _outputs(dp, torch.float32)
-    call = lambda: api.mla_dcp_decode_partial_noalloc(
-        dp.q_abs, dp.q_pe, dp.cache, dp.table, dp.lens, 1, o_part=o, lse_part=l,
-        scale=dp.prob.cfg.scale, err_flag=dp.err)
-    if need_fp32 > SCRATCH_BYTES:
-        with pytest.raises(api._ffi.MlaError) as e:
-            call()
-        assert e.value.status == 2
-    else:
-        call()
+    ws = None if need_fp32 > SCRATCH_BYTES else "default"
+    ref_o, ref_l = dp.partial(part_dtype=torch.float32, workspace=ws)
+    for _ in range(2):
+        o, l = _outputs(dp, torch.float32)
+        api.mla_dcp_decode_partial_noalloc(
+            dp.q_abs, dp.q_pe, dp.cache, dp.table, dp.lens, 1, o_part=o, lse_part=l,
+            scale=dp.prob.cfg.scale, err_flag=dp.err)
         torch.cuda.synchronize()
-        ref_o, ref_l = dp.partial(part_dtype=torch.float32)
+        assert dp.err.item() == 0
         assert torch.equal(o, ref_o) and torch.equal(l, ref_l)
+
+
+def test_noalloc_checks_arguments_like_the_workspace_entry_point():
+    """Bad arguments get the same status from both entry points."""
+    dp = DeviceProblem(inputs.make_problem(CASES["ragged"]))
+    o, l = _outputs(dp, dp.part_dt)
+    for kw in (dict(num_shards=65), dict(scale=-1.0)):
+        args = dict(num_shards=dp.prob.cfg.num_shards, scale=dp.prob.cfg.scale)
+        args.update(kw)
+        with pytest.raises(api._ffi.MlaError) as e1:
+            api.mla_dcp_decode_partial(dp.q_abs, dp.q_pe, dp.cache, dp.table, dp.lens,
+                                       args["num_shards"], kv_cur=dp.kv_cur, scale=args["scale"],
+                                       o_part=o, lse_part=l)
+        with pytest.raises(api._ffi.MlaError) as e2:
+            api.mla_dcp_decode_partial_noalloc(dp.q_abs, dp.q_pe, dp.cache, dp.table, dp.lens,
+                                               args["num_shards"], o_part=o, lse_part=l,
+                                               kv_cur=dp.kv_cur, scale=args["scale"])
+        assert e1.value.status == e2.value.status
