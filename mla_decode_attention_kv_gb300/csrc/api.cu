@@ -168,7 +168,6 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
   }
 
   mla::PartialParams pp;
-  pp.kv_base = static_cast<const uint8_t*>(kv_cache);
   pp.block_table = block_table;
   pp.seq_lens = seq_lens;
   pp.o_part = o_part;

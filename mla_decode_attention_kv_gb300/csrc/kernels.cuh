@@ -8,7 +8,6 @@
 namespace mla {
 
 struct PartialParams {
-  const uint8_t* kv_base;  // kv_cache (for the L2 prefetch of upcoming pages)
   const int32_t* block_table;
   const int32_t* seq_lens;
   void* o_part;

@@ -161,12 +161,21 @@ struct TileIter {
 };
 
 // Shared-memory plan (offsets from a 1024-aligned base; same size on both
-// ranks).  Rank 0: K chunk ring, Q RoPE tile, two outgoing P messages.
+// ranks).  Rank 0: K ring, Q RoPE tile, one outgoing P message.
 // Rank 1: V ring, two incoming P messages.  Barriers at one common offset.
+//
+// A ring stage is one mbarrier phase.  Each phase costs an SM a fixed few
+// hundred nanoseconds however many bytes it carries (measured on GB300: a
+// TMA stream with 8 KB per phase reaches 25 GB/s per SM, with 64 KB per
+// phase the full HBM rate from half the SMs), so the K ring moves three
+// 64-dim chunks (48 KB) per phase: a 128-token tile is exactly 3 stages.
 struct PairSmem {
   static constexpr int kTile = 128;
-  static constexpr int kKStage = kTile * 128;          // one 64-dim chunk of a tile
-  static constexpr int kNK = 10;
+  static constexpr int kKChunk = kTile * 128;          // one 64-dim chunk of a tile
+  static constexpr int kKPer = 3;                      // chunks per K stage
+  static constexpr int kKStage = kKPer * kKChunk;      // 48 KB
+  static constexpr int kNK = 3;                        // K stages: one tile
+  static constexpr int kQStages = (8 + kKPer - 1) / kKPer;   // stages of a query's 8 latent chunks
   static constexpr int kVSub = 32;                     // tokens per V stage
   static constexpr int kVChunk = kVSub * 128;          // one 64-dim chunk of a V stage
   static constexpr int kVStage = 8 * kVChunk;          // 32 tokens x 512 latent
@@ -182,15 +191,17 @@ struct PairSmem {
   static constexpr int kMsgStride = 34816;             // 1024-aligned slot
   // rank 0
   static constexpr int kKOff = 0;
-  static constexpr int kQrOff = kKOff + kNK * kKStage;       // 163840
-  static constexpr int kPsOff = kQrOff + 16384;              // 180224 (one outgoing message)
+  static constexpr int kQrOff = kKOff + kNK * kKStage;       // 147456
+  static constexpr int kPsOff = kQrOff + 16384;              // 163840 (one outgoing message)
+  static constexpr int kEnd0 = kPsOff + kMsgStride;          // 198656
   // rank 1
   static constexpr int kVOff = 0;
   static constexpr int kPrOff = kVOff + kNV * kVStage;       // 131072
-  static constexpr int kBarOff = kPsOff + kMsgStride;        // 215040
+  static constexpr int kEnd1 = kPrOff + 2 * kMsgStride;      // 200704
+  static constexpr int kBarOff = kEnd0 > kEnd1 ? kEnd0 : kEnd1;
   static constexpr int kTotal = kBarOff + 512 + 1024;
 };
-static_assert(PairSmem::kPrOff + 2 * PairSmem::kMsgStride <= PairSmem::kBarOff, "rank-1 plan");
+static_assert(9 == PairSmem::kNK * PairSmem::kKPer, "a tile's 9 chunks fill the K ring's stages exactly");
 static_assert(PairSmem::kTotal <= 232448, "shared memory budget");
 
 // Barrier slots in the common block.
@@ -215,12 +226,9 @@ enum : int {
   B_MMA_DONE_B = B_O_FIXED + 1,
   B_COUNT = B_MMA_DONE_B + 1
 };
-// barriers + TMEM slot + abort flag + 4 warp flags + 8 Q-chunk counters +
-// the producer's tile count must fit the barrier block
-static_assert((B_COUNT + 9) * 8 <= 512, "barrier block");
-
-// Tiles the QK CTA's L2 prefetch runs ahead of its TMA producer.
-constexpr int kPrefetchAhead = 2;
+// barriers + TMEM slot + abort flag + 4 warp flags + Q-stage counters must
+// fit the barrier block
+static_assert((B_COUNT + 4) * 8 + 32 <= 512, "barrier block");
 
 template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
@@ -244,8 +252,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + B_COUNT + 1);
   volatile uint32_t* warp_flags = reinterpret_cast<volatile uint32_t*>(bar + B_COUNT + 2);
-  int* q_readers = reinterpret_cast<int*>(bar + B_COUNT + 4);   // warps done with Q chunk c
-  volatile int* k_progress = reinterpret_cast<volatile int*>(bar + B_COUNT + 8);   // tiles issued
+  int* q_readers = reinterpret_cast<int*>(bar + B_COUNT + 4);   // warps done with Q stage
 
   const uint32_t rank = cluster_ctarank();
   const int warp = threadIdx.x >> 5;
@@ -267,7 +274,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         mbar_init(&bar[B_PFREE + k], 1);
       }
       mbar_init(&bar[B_MMA_DONE_A], 1);
-      for (int c = 0; c < 8; ++c) q_readers[c] = 0;
+      for (int c = 0; c < PairSmem::kQStages; ++c) q_readers[c] = 0;
     } else {
       for (int s = 0; s < L::kNV; ++s) {
         mbar_init(&bar[B_VFULL + s], 1);
@@ -286,7 +293,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       mbar_arrive_expect_tx(&bar[B_P_FULL + 1], L::kMsgBytes);
     }
     *abort_flag = 0;
-    *k_progress = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -483,7 +489,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       it.start(pp, rng);
       int cs = 0;
       int qloads = 0;
-      int ntile = 0;
       bool ok = true;
       const int nbox = TILE / br_k;      // boxes per chunk of a tile (1, 2 or 8)
       const bool boxlane = lane < nbox;
@@ -496,16 +501,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         if (it.first() && it.newq) {
           const int qrow = (ui.b * pp.q_len + ui.i) * pp.H;
           // Q latent of the new query: eight 64-column chunks through the
-          // ring, ahead of the unit's K (the softmax warps move them to TMEM)
-          for (int c = 0; c < 8; ++c) {
+          // ring (3 + 3 + 2 per stage), ahead of the unit's K (the softmax
+          // warps move them to TMEM)
+          for (int qs = 0; qs < L::kQStages; ++qs) {
             const int st = cs % L::kNK;
             if (cs >= L::kNK && !wait(&bar[B_KEMPTY + st], ((cs / L::kNK) - 1) & 1)) {
               ok = false;
               break;
             }
+            const int nc = min(L::kKPer, 8 - qs * L::kKPer);
             if (lane == 0) {
-              mbar_arrive_expect_tx(&bar[B_KFULL + st], L::kKStage);
-              tma_load_2d(sK + st * L::kKStage, &tm_qlat, &bar[B_KFULL + st], c * 64, qrow, pol_q);
+              mbar_arrive_expect_tx(&bar[B_KFULL + st], nc * L::kKChunk);
+              for (int k = 0; k < nc; ++k)
+                tma_load_2d(sK + st * L::kKStage + k * L::kKChunk, &tm_qlat, &bar[B_KFULL + st],
+                            (qs * L::kKPer + k) * 64, qrow, pol_q);
             }
             ++cs;
           }
@@ -522,20 +531,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         const int row = boxlane ? box_row(it, br_k, lane, id_cur) : 0;
         const CUtensorMap* map = ui.current ? &tm_cur : &tm_kv;
         uint8_t* dst = sK + lane * br_k * 128;
-        for (int c = 0; c < 9; ++c) {
+        for (int ks = 0; ks < L::kNK; ++ks) {
           const int st = cs % L::kNK;
           if (cs >= L::kNK && !wait(&bar[B_KEMPTY + st], ((cs / L::kNK) - 1) & 1)) {
             ok = false;
             break;
           }
           if (lane == 0) mbar_arrive_expect_tx(&bar[B_KFULL + st], L::kKStage);
-          if (boxlane)
-            tma_load_2d(dst + st * L::kKStage, map, &bar[B_KFULL + st], c * 64, row,
-                        c < 8 ? pol_kv : pol_rope);
+          if (boxlane) {
+#pragma unroll
+            for (int k = 0; k < L::kKPer; ++k) {
+              const int c = ks * L::kKPer + k;
+              tma_load_2d(dst + st * L::kKStage + k * L::kKChunk, map, &bar[B_KFULL + st], c * 64,
+                          row, c < 8 ? pol_kv : pol_rope);
+            }
+          }
           ++cs;
         }
         if (!ok) break;
-        if (lane == 0) *k_progress = ++ntile;   // paces the L2 prefetch warp
         id_cur = id_next;
         it = nx;
       }
@@ -563,23 +576,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
               ok = false;
               break;
             }
-            cs += 8;   // the Q latent chunks in the ring are the softmax warps' to free
+            cs += L::kQStages;   // the Q latent stages in the ring are the softmax warps' to free
           }
           const int sb = g & 1;
           if (g >= 2 && !wait(&bar[B_S_EMPTY + sb], ((g >> 1) - 1) & 1)) { ok = false; break; }
           const uint32_t d = tmem + kSCol + sb * TILE;
-          for (int c = 0; c < 9; ++c) {
+          for (int ks = 0; ks < L::kNK; ++ks) {
             const int st = cs % L::kNK;
             if (!wait(&bar[B_KFULL + st], (cs / L::kNK) & 1)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t kb = k_base + st * L::kKStage;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bd = make_desc_sw128(kb + kk * 32, 16, 1024);
-              if (c < 8)
-                umma_ts(d, tmem + kQlatCol + c * 32 + kk * 8, bd, idesc, (c | kk) ? 1u : 0u);
-              else
-                umma_ss(d, make_desc_sw128(qr_base + kk * 32, 16, 1024), bd, idesc, 1u);
+            for (int k = 0; k < L::kKPer; ++k) {
+              const int c = ks * L::kKPer + k;
+              const uint32_t kb = k_base + st * L::kKStage + k * L::kKChunk;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd = make_desc_sw128(kb + kk * 32, 16, 1024);
+                if (c < 8)
+                  umma_ts(d, tmem + kQlatCol + c * 32 + kk * 8, bd, idesc, (c | kk) ? 1u : 0u);
+                else
+                  umma_ss(d, make_desc_sw128(qr_base + kk * 32, 16, 1024), bd, idesc, 1u);
+              }
             }
             umma_commit(&bar[B_KEMPTY + st]);
             ++cs;
@@ -602,45 +619,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         const int64_t row0 = (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H;
         for (int h = t; h < pp.H; h += 64) pp.lse_part[row0 + h] = -INFINITY;
       }
-      if (warp == 2) {
-        // ---------------------------------------------- rank 0: L2 prefetch
-        // Walks the pair's tiles kPrefetchAhead ahead of the TMA producer and
-        // asks L2 for each box's rows (one contiguous run of a page), so the
-        // ring's loads find their data in L2: the ring then only has to
-        // cover L2 latency, not HBM latency.  Lane l takes box l, as the
-        // producer does; a box never crosses a page.  Prefetch is a hint:
-        // bad block ids are left for the producer to report, and the warp
-        // stops (without an error) if it ever waits too long.
-        TileIter<TILE> pf;
-        pf.start(pp, rng);
-        const int nbox = TILE / br_k;
-        int g = 0;
-        while (pf.valid) {
-          bool go = true;
-          for (uint32_t spin = 0; g - *k_progress > kPrefetchAhead; ++spin) {
-            if (spin >= kSpinLimit || *abort_flag) {
-              go = false;
-              break;
-            }
-            __nanosleep(128);
-          }
-          if (!go) break;
-          if (lane < nbox && !pf.ui.current) {
-            const int tk = pf.ui.lo + pf.j * TILE + lane * br_k;
-            if (tk < pf.ui.hi) {
-              const int id = __ldg(pp.block_table + static_cast<int64_t>(pf.ui.b) * pp.max_blocks +
-                                   (tk >> bs_shift));
-              if (id >= 0 && id < pp.num_blocks) {
-                const int64_t row = (static_cast<int64_t>(id) << bs_shift) + (tk & (pp.bs - 1));
-                const int rows = min(br_k, pf.ui.hi - tk);
-                prefetch_l2(pp.kv_base + row * 1152, static_cast<uint32_t>(rows) * 1152u);
-              }
-            }
-          }
-          pf.advance(pp);
-          ++g;
-        }
-      }
     } else {
       // ------------------------------------------------ rank 0: softmax
       const int r = threadIdx.x - 128;           // TMEM lane == head row
@@ -651,7 +629,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       TileIter<TILE> it;
       it.start(pp, rng);
       int g = 0;
-      int cq = 0;   // ring position: 8 Q chunks per new query, 9 K chunks per tile
+      int cq = 0;   // ring position in stages: kQStages per new query, kNK per tile
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       while (ok && it.valid) {
@@ -666,15 +644,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             if (!named_bar_and(1, 128, qe)) { ok = false; break; }
             tc_fence_after();
             // each warp copies its 32 rows of a chunk; the last warp done
-            // with a chunk frees its stage (no block-wide barrier per chunk)
+            // with a stage frees it (no block-wide barrier per stage)
             for (int c = 0; c < 8; ++c) {
-              const int st = (cq + c) % L::kNK;
-              if (!wait_lazy(&bar[B_KFULL + st], ((cq + c) / L::kNK) & 1)) {
+              const int qs = c / L::kKPer, k = c % L::kKPer;
+              const int st = (cq + qs) % L::kNK;
+              if (k == 0 && !wait_lazy(&bar[B_KFULL + st], ((cq + qs) / L::kNK) & 1)) {
                 ok = false;
                 break;
               }
-              // row r of a 128-byte-swizzled stage: 16-byte unit j at (j ^ (r & 7))
-              const uint8_t* rowp = sK + st * L::kKStage + r * 128;
+              // row r of a 128-byte-swizzled chunk: 16-byte unit j at (j ^ (r & 7))
+              const uint8_t* rowp = sK + st * L::kKStage + k * L::kKChunk + r * 128;
               uint32_t w[32];
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
@@ -686,16 +665,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 w[4 * j + 3] = x.w;
               }
               tmem_st32(tmem + lane_base + kQlatCol + c * 32, w);   // consumes the loads
-              __syncwarp();
-              if (lane == 0) {
-                __threadfence_block();
-                if (atomicAdd(&q_readers[c], 1) == 3) {
-                  q_readers[c] = 0;
-                  mbar_arrive(&bar[B_KEMPTY + st]);
+              if (k == L::kKPer - 1 || c == 7) {
+                __syncwarp();
+                if (lane == 0) {
+                  __threadfence_block();
+                  if (atomicAdd(&q_readers[qs], 1) == 3) {
+                    q_readers[qs] = 0;
+                    mbar_arrive(&bar[B_KEMPTY + st]);
+                  }
                 }
               }
             }
-            cq += 8;
+            cq += L::kQStages;
             if (!named_bar_and(1, 128, ok)) { ok = false; break; }
             tmem_wait_st();
             tc_fence_before();
@@ -793,7 +774,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         ok = named_bar_and(1, 128, ok && !*abort_flag);
         it.advance(pp);
         ++g;
-        cq += 9;
+        cq += L::kNK;
       }
       if (threadIdx.x == 128) bulk_wait_read<0>();
     }
