@@ -16,7 +16,7 @@ struct PartialParams {
   int B, q_len, H, num_blocks, bs, max_blocks, S, P, has_cur;
   int num_units;
   int box_rows;          // rows per TMA box of the QK CTA's KV maps: min(128, block_size)
-  int box_rows_v;        // rows per TMA box of the PV CTA's KV maps: min(32, block_size)
+  int box_rows_v;        // rows per TMA box of the PV CTA's KV maps: min(64, block_size)
   float scale_log2;      // softmax scale * log2(e)
   int part_dtype;        // 0 bf16, 1 fp16, 2 fp32
   // Split-unit workspace (split = number of CTA pairs, 0 = whole units):
@@ -39,9 +39,9 @@ inline size_t partial_workspace_bytes(int clusters, int part_bytes = 4) {
 int partial_max_clusters();
 
 // Rows per TMA box of the partial kernel's KV maps: min(box, block_size) for
-// the QK CTA (128-token tiles) and the PV CTA (32-token stages).
+// the QK CTA (128-token tiles) and the PV CTA (64-token stages).
 constexpr int kPartialBoxK = 128;
-constexpr int kPartialBoxV = 32;
+constexpr int kPartialBoxV = 64;
 
 int launch_partial(const CUtensorMap& qlat, const CUtensorMap& qpe, const CUtensorMap& kv,
                    const CUtensorMap& cur, const CUtensorMap& kv_v, const CUtensorMap& cur_v,

@@ -176,10 +176,10 @@ struct PairSmem {
   static constexpr int kKStage = kKPer * kKChunk;      // 48 KB
   static constexpr int kNK = 3;                        // K stages: one tile
   static constexpr int kQStages = (8 + kKPer - 1) / kKPer;   // stages of a query's 8 latent chunks
-  static constexpr int kVSub = 32;                     // tokens per V stage
+  static constexpr int kVSub = 64;                     // tokens per V stage
   static constexpr int kVChunk = kVSub * 128;          // one 64-dim chunk of a V stage
-  static constexpr int kVStage = 8 * kVChunk;          // 32 tokens x 512 latent
-  static constexpr int kNV = 4;
+  static constexpr int kVStage = 8 * kVChunk;          // 64 tokens x 512 latent (64 KB)
+  static constexpr int kNV = 2;
   // P message: P [128 rows x 128 tokens] as two 64-token SW128 chunks,
   // alpha[128], lsum[128], header.
   static constexpr int kMsgP = 2 * 16384;
@@ -482,9 +482,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       // The whole warp runs the loop converged: every lane polls the stage
       // barrier and lane l issues box l of each chunk (no shuffles, no
       // divergent single-lane sections on the issue path).
-      const uint64_t pol_kv = policy_evict_last();     // rank 1 re-reads the latent
-      const uint64_t pol_rope = policy_evict_first();  // chunk 8 (k_R): read once
-      const uint64_t pol_q = policy_evict_last();
       TileIter<TILE> it;
       it.start(pp, rng);
       int cs = 0;
@@ -514,7 +511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
               mbar_arrive_expect_tx(&bar[B_KFULL + st], nc * L::kKChunk);
               for (int k = 0; k < nc; ++k)
                 tma_load_2d(sK + st * L::kKStage + k * L::kKChunk, &tm_qlat, &bar[B_KFULL + st],
-                            (qs * L::kKPer + k) * 64, qrow, pol_q);
+                            (qs * L::kKPer + k) * 64, qrow);
             }
             ++cs;
           }
@@ -523,7 +520,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           if (it.nq >= 1 && !wait(&bar[B_Q_EMPTY], (it.nq - 1) & 1)) break;
           if (lane == 0) {
             mbar_arrive_expect_tx(&bar[B_QR_FULL], 16384);
-            tma_load_2d(sQr, &tm_qpe, &bar[B_QR_FULL], 0, qrow, pol_q);
+            tma_load_2d(sQr, &tm_qpe, &bar[B_QR_FULL], 0, qrow);
           }
           ++qloads;
         }
@@ -543,7 +540,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             for (int k = 0; k < L::kKPer; ++k) {
               const int c = ks * L::kKPer + k;
               tma_load_2d(dst + st * L::kKStage + k * L::kKChunk, map, &bar[B_KFULL + st], c * 64,
-                          row, c < 8 ? pol_kv : pol_rope);
+                          row);
             }
           }
           ++cs;
@@ -785,7 +782,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       // ------------------------------------------------ rank 1: TMA producer (V)
       // Converged warp: lane (bb * 8 + c) issues latent chunk c of box bb of
       // each 32-token stage; lanes 0..nbox-1 hold the tile's box rows.
-      const uint64_t pol_kv = policy_evict_first();    // second and last reader
       TileIter<TILE> it;
       it.start(pp, rng);
       int vs = 0;
@@ -813,7 +809,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           }
           if (lane == 0) mbar_arrive_expect_tx(&bar[B_VFULL + st], L::kVStage);
           if (vlane)
-            tma_load_2d(dst + st * L::kVStage, map, &bar[B_VFULL + st], vc * 64, row, pol_kv);
+            tma_load_2d(dst + st * L::kVStage, map, &bar[B_VFULL + st], vc * 64, row);
           ++vs;
         }
         if (!ok) break;
