@@ -257,6 +257,19 @@ int mla_gather_kv(const void* kv_cache, const int32_t* block_table, const int32_
                   int B, int num_blocks, int block_size, int max_blocks, int max_len,
                   void* dst, int32_t* err_flag, mla_stream_t stream);
 
+/*
+ * mla_debug_set_spin_limit -- test hook for the device error path: the
+ * number of polls after which a pipeline wait of mla_dcp_decode_partial (and
+ * of mla_dcp_decode_partial_noalloc) gives up and records
+ * MLA_DEV_WAIT_TIMEOUT; 0 restores the default of 2^22 polls.  It applies
+ * to every call launched after it, from any host thread.  With a limit short
+ * enough to run out, that call's outputs are unspecified and *err_flag reads
+ * MLA_DEV_WAIT_TIMEOUT; the kernel still waits for its own copies and MMAs
+ * already issued, frees its tensor memory and returns, so the CUDA context
+ * stays usable.  A library addition with no counterpart in the sources.
+ */
+void mla_debug_set_spin_limit(uint32_t polls);
+
 /* Human-readable text of an mla_status or device error code. */
 const char* mla_get_error_string(int status);
 const char* mla_device_error_string(int code);

@@ -32,6 +32,7 @@ SIGNATURES = {
     "mla_get_error_string": (ctypes.c_char_p, [I]),
     "mla_device_error_string": (ctypes.c_char_p, [I]),
     "mla_version": (I, []),
+    "mla_debug_set_spin_limit": (None, [ctypes.c_uint32]),
 }
 
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_NULL_POINTER", 2: "MLA_ERR_BAD_SHAPE",

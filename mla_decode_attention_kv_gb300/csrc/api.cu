@@ -5,9 +5,11 @@
 #include <cuda_runtime.h>
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 #include "../../include/mla_dcp.h"
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace {
 
@@ -75,6 +77,23 @@ int launched(int rc) {
 extern "C" {
 
 int mla_version(void) { return 100; }
+
+}  // extern "C"
+
+namespace {
+std::atomic<uint32_t> g_spin_limit{0};   // 0: the kernels' default
+}  // namespace
+
+uint32_t mla::partial_spin_limit() {
+  const uint32_t v = g_spin_limit.load(std::memory_order_relaxed);
+  return v ? v : mla::kSpinLimit;
+}
+
+extern "C" {
+
+void mla_debug_set_spin_limit(uint32_t polls) {
+  g_spin_limit.store(polls, std::memory_order_relaxed);
+}
 
 const char* mla_get_error_string(int status) {
   switch (status) {
@@ -186,6 +205,7 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
   pp.box_rows = box_k;
   pp.box_rows_v = box_v;
   pp.scale_log2 = scale * 1.4426950408889634f;
+  pp.spin_limit = mla::partial_spin_limit();
   pp.part_dtype = part_dtype;
   pp.split = 0;
   pp.ws_o = nullptr;

@@ -18,6 +18,7 @@ struct PartialParams {
   int box_rows;          // rows per TMA box of the QK CTA's KV maps: min(128, block_size)
   int box_rows_v;        // rows per TMA box of the PV CTA's KV maps: min(64, block_size)
   float scale_log2;      // softmax scale * log2(e)
+  uint32_t spin_limit;   // polls before a pipeline wait gives up (MLA_DEV_WAIT_TIMEOUT)
   int part_dtype;        // 0 bf16, 1 fp16, 2 fp32
   // Split-unit workspace (split = number of CTA pairs, 0 = whole units):
   // per pair two slots of O / l and LSE (log2, [128]) for the units cut at
@@ -37,6 +38,9 @@ inline size_t partial_workspace_bytes(int clusters, int part_bytes = 4) {
   return recs + slots * 128 * 4 + slots * 512 * 128 * static_cast<size_t>(part_bytes);
 }
 int partial_max_clusters();
+// Polls before a pipeline wait of the partial kernel gives up: kSpinLimit
+// unless a test lowers it (mla_debug_set_spin_limit).
+uint32_t partial_spin_limit();
 
 // Rows per TMA box of the partial kernel's KV maps: min(box, block_size) for
 // the QK CTA (128-token tiles) and the PV CTA (64-token stages).

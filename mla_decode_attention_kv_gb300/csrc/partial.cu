@@ -224,11 +224,12 @@ enum : int {
   B_O_EMPTY = B_META_READ + 2,
   B_O_FIXED = B_O_EMPTY + 1,
   B_MMA_DONE_B = B_O_FIXED + 1,
-  B_COUNT = B_MMA_DONE_B + 1
+  B_MSG_FREE = B_MMA_DONE_B + 1,   // rank 0: the outgoing P message has landed in rank 1
+  B_COUNT = B_MSG_FREE + 1
 };
-// barriers + TMEM slot + abort flag + 4 warp flags + Q-stage counters must
-// fit the barrier block
-static_assert((B_COUNT + 4) * 8 + 32 <= 512, "barrier block");
+// barriers + TMEM slot + abort flag + 4 warp flags + Q-stage counters + the
+// P message count must fit the barrier block
+static_assert((B_COUNT + 9) * 8 <= 512, "barrier block");
 
 template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
@@ -253,6 +254,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + B_COUNT + 1);
   volatile uint32_t* warp_flags = reinterpret_cast<volatile uint32_t*>(bar + B_COUNT + 2);
   int* q_readers = reinterpret_cast<int*>(bar + B_COUNT + 4);   // warps done with Q stage
+  // rank 0: P messages sent; rank 1: P messages the PV issuer has seen land
+  volatile int* msg_count = reinterpret_cast<volatile int*>(bar + B_COUNT + 8);
 
   const uint32_t rank = cluster_ctarank();
   const int warp = threadIdx.x >> 5;
@@ -274,6 +277,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         mbar_init(&bar[B_PFREE + k], 1);
       }
       mbar_init(&bar[B_MMA_DONE_A], 1);
+      mbar_init(&bar[B_MSG_FREE], 1);
       for (int c = 0; c < PairSmem::kQStages; ++c) q_readers[c] = 0;
     } else {
       for (int s = 0; s < L::kNV; ++s) {
@@ -293,6 +297,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       mbar_arrive_expect_tx(&bar[B_P_FULL + 1], L::kMsgBytes);
     }
     *abort_flag = 0;
+    *msg_count = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -417,8 +422,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     rng.t_begin = static_cast<int>(lo);
   }
 
+  // Protocol waits give up after pp.spin_limit polls (the drains at the end
+  // of the kernel, which wait for copies and MMAs already issued, use the
+  // fixed kSpinLimit: those always complete).
+  const uint32_t spin_limit = pp.spin_limit;
   auto wait = [&](uint64_t* b, uint32_t parity) -> bool {
-    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    for (uint32_t it = 0; it < spin_limit; ++it) {
       if (mbar_try_wait(b, parity)) return true;
       if ((it & 1023u) == 1023u && *abort_flag) return false;
     }
@@ -428,7 +437,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   };
   // Waits of whole warp groups off the issue path: polls may suspend.
   auto wait_lazy = [&](uint64_t* b, uint32_t parity) -> bool {
-    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    for (uint32_t it = 0; it < spin_limit; ++it) {
       if (mbar_try_wait_sleep(b, parity, kLazyWaitNs)) return true;
       if ((it & 15u) == 15u && *abort_flag) return false;
     }
@@ -437,7 +446,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     return false;
   };
   auto wait_cl = [&](uint64_t* b, uint32_t parity) -> bool {
-    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    for (uint32_t it = 0; it < spin_limit; ++it) {
       if (mbar_try_wait_cluster(b, parity)) return true;
       if ((it & 1023u) == 1023u && *abort_flag) return false;
     }
@@ -734,9 +743,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
 
         // ---- P message for rank 1
-        uint8_t* msg = sPs;                           // single outgoing buffer
-        if (threadIdx.x == 128) bulk_wait_read<0>();   // copy of tile g-1 has read msg
-        named_bar_sync(1, 128);
+        // Single outgoing buffer: the copy of tile g-1 has finished reading
+        // it once that message has landed in rank 1, which rank 1 reports on
+        // B_MSG_FREE (a shared-to-cluster bulk copy completes only on the
+        // destination's mbarrier; no wait of the sender tracks it).
+        uint8_t* msg = sPs;
+        bool mfree = true;
+        if (threadIdx.x == 128 && g >= 1) mfree = wait_cl(&bar[B_MSG_FREE], (g - 1) & 1);
+        if (!named_bar_and(1, 128, mfree)) { ok = false; break; }
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -765,7 +779,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           if (ok) {
             bulk_copy_to_peer(precv_peer + sb * L::kMsgStride, msg, L::kMsgBytes,
                               pfull_peer + sb * 8);
-            bulk_commit();
+            *msg_count = g + 1;
           }
         }
         ok = named_bar_and(1, 128, ok && !*abort_flag);
@@ -773,7 +787,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         ++g;
         cq += L::kNK;
       }
-      if (threadIdx.x == 128) bulk_wait_read<0>();
     }
   } else {
     uint8_t* sV = smem + L::kVOff;
@@ -904,6 +917,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           }
         }
       }
+      // ------------------------------------------------ rank 1: P landing watcher
+      // Reports each P message to rank 0 as soon as it has landed (the
+      // sender's single buffer is then free) and counts them for the drain
+      // at the end of the kernel.  A message lands only in an armed slot,
+      // and rank 0 sends message g + 2 only after this report for g + 1, so
+      // the watcher can never fall a whole phase behind on a slot.
+      if (lane == 0) {
+        const uint32_t msgfree_peer = map_to_peer(&bar[B_MSG_FREE], 0);
+        TileIter<TILE> it;
+        it.start(pp, rng);
+        int g = 0;
+        while (it.valid) {
+          if (!wait(&bar[B_P_FULL + (g & 1)], (g >> 1) & 1)) break;
+          *msg_count = g + 1;
+          mbar_arrive_remote(msgfree_peer);
+          it.advance(pp);
+          ++g;
+        }
+      }
     } else {
       // ------------------------------------------------ rank 1: O rescale + epilogue
       const int r = threadIdx.x - 128;
@@ -993,6 +1025,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     }
   }
 
+  // every tensor-memory access of this thread has completed (a warp that left
+  // the Q copy early may still have stores in flight) before TMEM is freed
+  __syncwarp();
+  tmem_wait_st();
+  tmem_wait_ld();
   tc_fence_before();
   __syncthreads();
   if (pp.split && rank == 1 && threadIdx.x == 0) {
@@ -1009,6 +1046,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     }
     pp.ws_units[cid] = rec;
     if (cid == 0) pp.ws_units[ncl] = make_int4(static_cast<int>(share_total), ncl, 0, 0);
+  }
+  cluster_sync();
+  if (rank == 1 && threadIdx.x == 64) {
+    // Drain the P messages rank 0 sent that the PV issuer never saw land
+    // (it stops early when a wait runs out): rank 0 must not exit while its
+    // copies still read its buffer, nor rank 1 while they still write here.
+    // Every message went to an armed slot, so each completes a P_FULL phase.
+    const uint32_t sent_addr = map_to_peer(const_cast<int*>(msg_count), 0);
+    int sent;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(sent) : "r"(sent_addr) : "memory");
+    for (int k = *msg_count; k < sent; ++k) mbar_wait(&bar[B_P_FULL + (k & 1)], (k >> 1) & 1, err);
   }
   cluster_sync();   // no DSMEM traffic into either CTA after this point
   if (warp == 1) {

@@ -420,6 +420,33 @@ def test_bad_seq_len_sets_device_error(bad):
     _check_partials(dp2, o_part, lse_part)
 
 
+def test_wait_timeout_sets_device_error_and_context_survives():
+    """The failure path of a pipeline wait, made to run out on purpose: with
+    the waits' poll budget cut to a few polls (a test hook, nothing faults),
+    the partial kernel records MLA_DEV_WAIT_TIMEOUT, drains what it issued and
+    returns; a normal call on the same context then matches the oracle.  Both
+    work splits (with and without a workspace) and two calls in a row."""
+    lib = api._ffi.lib()
+    dp = DeviceProblem(inputs.make_problem(SMALL["ragged_bf16_cur"]))
+    try:
+        lib.mla_debug_set_spin_limit(8)
+        for ws in ("default", None, "default"):
+            dp.err.zero_()
+            dp.partial(workspace=ws)
+            torch.cuda.synchronize()
+            assert dp.err.item() == 2
+    finally:
+        lib.mla_debug_set_spin_limit(0)
+    dp.err.zero_()
+    o_part, lse_part = dp.partial()
+    out = api.mla_lse_combine_vup(o_part, lse_part, dp.W, err_flag=dp.err)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    _check_partials(dp, o_part, lse_part)
+    _, _, ref_out = om.decode_reference(dp.prob)
+    assert_out_close(f64(out), ref_out, "out")
+
+
 def test_host_errors_launch_nothing():
     dp = DeviceProblem(inputs.make_problem(inputs.CONFIGS["tiny"]))
     with pytest.raises(api._ffi.MlaError) as e:
