@@ -77,7 +77,12 @@ enum {
   MLA_D_QK = 576,     /* values per cached token ([TP] route A, ~1.15 KB/token) */
   MLA_D_V = 128,      /* per-head V width after the up-projection ([PR] block A) */
   MLA_MAX_HEADS = 128,
-  MLA_MAX_SHARDS = 64
+  MLA_MAX_SHARDS = 64,
+  /* query tokens per sequence: decode (1), MTP (2) and CURRENT chunks of a
+   * chunked prefill up to 64 ([PR] closing paragraph of the proposal keeps
+   * prefill itself on the old path); the CURRENT part of query i covers
+   * kv_cur[b, 0..i], one KV tile of the partial kernel */
+  MLA_MAX_Q_LEN = 64
 };
 
 /*
@@ -111,7 +116,7 @@ enum {
  *   seq_lens   [B] int32 (device)  history lengths, 0 <= L_b <= max_blocks*block_size;
  *              an entry outside that range sets MLA_DEV_BAD_SEQ_LEN
  *   kv_cur     [B, q_len, 576] in_dtype, or NULL (no CURRENT segment)
- *   B >= 1; 1 <= q_len <= 8; 1 <= H <= 128; block_size in {16,32,64,128,256};
+ *   B >= 1; 1 <= q_len <= 64; 1 <= H <= 128; block_size in {16,32,64,128,256};
  *   1 <= num_shards <= 64; scale > 0 (1/sqrt(192) for the 128+64 head width)
  *   in_dtype   MLA_BF16 or MLA_FP16;  part_dtype MLA_BF16, MLA_FP16 or MLA_FP32
  *   o_part     [B, q_len, P, H, 512] part_dtype, P = num_shards + (kv_cur != NULL)

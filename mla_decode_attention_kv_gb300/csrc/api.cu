@@ -131,7 +131,7 @@ int check_partial_args(const void* q_abs, const void* q_pe, const void* kv_cache
   if (!q_abs || !q_pe || !kv_cache || !block_table || !seq_lens || !o_part || !lse_part)
     return MLA_ERR_NULL_POINTER;
   if (!is_half_dtype(in_dtype) || !is_part_dtype(part_dtype)) return MLA_ERR_BAD_DTYPE;
-  if (B < 1 || q_len < 1 || q_len > 8 || H < 1 || H > MLA_MAX_HEADS || num_blocks < 1 ||
+  if (B < 1 || q_len < 1 || q_len > MLA_MAX_Q_LEN || H < 1 || H > MLA_MAX_HEADS || num_blocks < 1 ||
       max_blocks < 1 || !(scale > 0.f) || !std::isfinite(scale))
     return MLA_ERR_BAD_SHAPE;
   if (num_shards < 1 || num_shards > MLA_MAX_SHARDS) return MLA_ERR_BAD_SHARDS;
@@ -228,7 +228,7 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
 }
 
 uint64_t mla_dcp_decode_partial_workspace_size(int B, int q_len, int num_shards, int has_current) {
-  if (B < 1 || q_len < 1 || q_len > 8 || num_shards < 1 || num_shards > MLA_MAX_SHARDS) return 0;
+  if (B < 1 || q_len < 1 || q_len > MLA_MAX_Q_LEN || num_shards < 1 || num_shards > MLA_MAX_SHARDS) return 0;
   const int64_t units = static_cast<int64_t>(B) * q_len * (num_shards + (has_current ? 1 : 0));
   if (units > INT32_MAX) return 0;
   const int clusters = mla::partial_max_clusters();

@@ -64,6 +64,7 @@ def test_partial_host_checks(lib):
     assert _partial(lib, pdt=7) == 3
     assert _partial(lib, H=129) == 2
     assert _partial(lib, q=0) == 2
+    assert _partial(lib, q=65) == 2
     assert _partial(lib, scale=0.0) == 2
     assert _partial(lib, S=0) == 5
     assert _partial(lib, S=65) == 5
@@ -74,7 +75,7 @@ def test_partial_host_checks(lib):
 
 def test_workspace_size_rejects_bad_sizes(lib):
     assert lib.mla_dcp_decode_partial_workspace_size(0, 1, 2, 0) == 0
-    assert lib.mla_dcp_decode_partial_workspace_size(2, 9, 2, 0) == 0
+    assert lib.mla_dcp_decode_partial_workspace_size(2, 65, 2, 0) == 0
     assert lib.mla_dcp_decode_partial_workspace_size(2, 1, 65, 1) == 0
 
 

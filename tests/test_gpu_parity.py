@@ -277,6 +277,23 @@ def test_many_query_tokens_few_heads():
     assert_out_close(f64(out), ref_out, "out")
 
 
+@pytest.mark.parametrize("q_len,bs", [(16, 32), (64, 16), (64, 64)])
+def test_long_current_chunk(q_len, bs):
+    """CURRENT chunks of 16 and 64 query tokens (a chunked-prefill step)
+    with 128 heads: query i sees history plus current tokens 0..i; every
+    shard partial, the CURRENT partial and the combined output."""
+    cfg = inputs.DecodeConfig(name=f"q{q_len}", batch=2, heads=128, q_len=q_len, num_shards=2,
+                              block_size=bs, ragged=(60, 500), current=True, seed=141 + q_len)
+    dp = DeviceProblem(inputs.make_problem(cfg))
+    o_part, lse_part = dp.partial()
+    out = api.mla_lse_combine_vup(o_part, lse_part, dp.W, err_flag=dp.err)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    _check_partials(dp, o_part, lse_part)
+    _, _, ref_out = om.decode_reference(dp.prob)
+    assert_out_close(f64(out), ref_out, "out")
+
+
 @pytest.mark.parametrize("batch,shards", [(3, 4), (32, 8), (5, 64)])
 def test_all_parts_empty(batch, shards):
     """No history and no CURRENT chunk: every partial is o = 0, lse = -inf,
