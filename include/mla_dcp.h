@@ -144,6 +144,29 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
                            mla_stream_t stream);
 
 /*
+ * mla_dcp_decode_partial_sliced -- mla_dcp_decode_partial with its partials
+ * laid out for an exchange between GPUs that scatters heads.
+ *
+ * Defines: [PR] the third change (the HISTORY partials of every rank go
+ * through one all-to-all with scatter_dim = 1, the heads, before the
+ * combine).  With head_slices = N (dividing H), o_part is
+ * [N][B*q_len][P][H/N][512] and lse_part [N][B*q_len][P][H/N]: head h of
+ * token t = b*q_len + i, part p is row ((h / (H/N)) * B*q_len + t) * P + p)
+ * * (H/N) + h % (H/N).  Block n (heads [n*H/N, (n+1)*H/N)) is contiguous,
+ * so it is exactly what rank n receives from an all-to-all of equal
+ * splits.  head_slices = 1 is mla_dcp_decode_partial.  Every other argument,
+ * result and error as mla_dcp_decode_partial; MLA_ERR_BAD_SHAPE if
+ * head_slices < 1 or does not divide H.
+ */
+int mla_dcp_decode_partial_sliced(const void* q_abs, const void* q_pe, const void* kv_cache,
+                                  const int32_t* block_table, const int32_t* seq_lens,
+                                  const void* kv_cur, int B, int q_len, int H, int num_blocks,
+                                  int block_size, int max_blocks, int num_shards, float scale,
+                                  int in_dtype, int part_dtype, void* o_part, float* lse_part,
+                                  int32_t* err_flag, void* workspace, uint64_t workspace_bytes,
+                                  int head_slices, mla_stream_t stream);
+
+/*
  * mla_dcp_decode_partial_workspace_size -- bytes of workspace that
  * mla_dcp_decode_partial needs on the current device: about 0.5 MiB per
  * CTA pair the device keeps resident (FP32 partials need twice that), with
@@ -210,6 +233,31 @@ int mla_dcp_decode_partial_noalloc(const void* q_abs, const void* q_pe, const vo
 int mla_lse_combine(const void* o_part, const float* lse_part, int num_parts,
                     const void* o_local, const float* lse_local, int T, int H, int part_dtype,
                     int out_dtype, void* o_latent, float* lse_out, mla_stream_t stream);
+
+/*
+ * mla_dcp_combine_exchanged -- the combine on one GPU after the exchange
+ * between GPUs.
+ *
+ * Defines: [PR] the third and fourth changes: after the head-scattered
+ * all-to-all each rank combines, for its slice of heads, the HISTORY
+ * partials of all ranks plus the CURRENT partial exactly once (the local
+ * output / local LSE).  o_recv [num_src][T][parts_per_src][H][512] and
+ * lse_recv [num_src][T][parts_per_src][H] are what the all-to-all delivered
+ * (block src = the sliced partials of rank src for this rank's heads, H =
+ * heads of the slice).  Parts p < hist_parts of every source are history
+ * shards; if local_src >= 0, part hist_parts of source local_src (the CURRENT
+ * partial, which every rank computes alike) is added once.
+ *   LSE = ln sum exp(lse_q);  o = sum exp(lse_q - LSE) o_q  over those parts
+ * in the order (src 0, p 0..), (src 1, ...), ..., then the local one; parts
+ * with lse = -inf carry no weight.
+ *   o_latent [T, H, 512] out_dtype;  lse_out [T, H] float32 or NULL
+ *   1 <= num_src * hist_parts (+1 with the local part) <= 96;
+ *   1 <= parts_per_src <= 65;  -1 <= local_src < num_src
+ */
+int mla_dcp_combine_exchanged(const void* o_recv, const float* lse_recv, int num_src,
+                              int parts_per_src, int hist_parts, int local_src, int T, int H,
+                              int part_dtype, int out_dtype, void* o_latent, float* lse_out,
+                              mla_stream_t stream);
 
 /*
  * mla_vup -- batch-major V up-projection.

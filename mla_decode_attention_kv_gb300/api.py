@@ -72,13 +72,16 @@ def partial_workspace(device, B: int, q_len: int, num_shards: int, has_current: 
 def mla_dcp_decode_partial(q_abs, q_pe, kv_cache, block_table, seq_lens, num_shards: int, *,
                            kv_cur=None, scale: float = DEFAULT_SCALE, part_dtype=None,
                            o_part=None, lse_part=None, err_flag=None, stream=None,
-                           workspace="default"):
+                           workspace="default", head_slices: int = 1):
     """Partial attention of every (sequence, query token, shard [, CURRENT]).
 
     q_abs [B, q, H, 512], q_pe [B, q, H, 64], kv_cache [num_blocks, bs, 576],
     block_table [B, max_blocks] int32, seq_lens [B] int32 (history lengths),
     kv_cur [B, q, 576] or None.  Returns o_part [B, q, P, H, 512] and
-    lse_part [B, q, P, H] (float32), P = num_shards + (kv_cur is not None).
+    lse_part [B, q, P, H] (float32), P = num_shards + (kv_cur is not None);
+    with head_slices = N > 1 they are [N, B*q, P, H/N, 512] and
+    [N, B*q, P, H/N] (mla_dcp_decode_partial_sliced: block n is what rank n
+    receives in a head-scattered all-to-all).
     workspace: "default" (one kept per device and stream, see
     partial_workspace), a uint8 CUDA tensor of at least
     mla_dcp_decode_partial_workspace_size bytes, or None (pairs of CTAs then
@@ -90,23 +93,51 @@ def mla_dcp_decode_partial(q_abs, q_pe, kv_cache, block_table, seq_lens, num_sha
     for t, n in ((q_abs, "q_abs"), (q_pe, "q_pe"), (kv_cache, "kv_cache"),
                  (block_table, "block_table"), (seq_lens, "seq_lens")):
         _need(t, n)
+    if head_slices == 1:
+        o_shape, l_shape = (B, q_len, P, H, D_LATENT), (B, q_len, P, H)
+    else:
+        hs = H // head_slices
+        o_shape = (head_slices, B * q_len, P, hs, D_LATENT)
+        l_shape = (head_slices, B * q_len, P, hs)
     if o_part is None:
-        o_part = torch.empty((B, q_len, P, H, D_LATENT), dtype=part_dtype, device=q_abs.device)
+        o_part = torch.empty(o_shape, dtype=part_dtype, device=q_abs.device)
     if lse_part is None:
-        lse_part = torch.empty((B, q_len, P, H), dtype=torch.float32, device=q_abs.device)
+        lse_part = torch.empty(l_shape, dtype=torch.float32, device=q_abs.device)
     if isinstance(workspace, str):
         if workspace != "default":
             raise ValueError("workspace must be 'default', a tensor or None")
         workspace = partial_workspace(q_abs.device, B, q_len, num_shards, kv_cur is not None,
                                       stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _ffi.lib().mla_dcp_decode_partial(
+    st = _ffi.lib().mla_dcp_decode_partial_sliced(
         _p(q_abs), _p(q_pe), _p(kv_cache), _p(block_table), _p(seq_lens), _p(kv_cur),
         B, q_len, H, num_blocks, bs, block_table.shape[1], num_shards, float(scale),
         _code(q_abs.dtype), _code(o_part.dtype), _p(o_part), _p(lse_part), _p(err_flag),
-        _p(workspace), ws_bytes, _s(stream))
-    _ffi.check("mla_dcp_decode_partial", st)
+        _p(workspace), ws_bytes, int(head_slices), _s(stream))
+    _ffi.check("mla_dcp_decode_partial_sliced", st)
     return o_part, lse_part
+
+
+def mla_dcp_combine_exchanged(o_recv, lse_recv, *, hist_parts: int, local_src: int = -1,
+                              out_dtype=None, o_latent=None, lse_out=None, stream=None):
+    """Combine on one GPU after the head-scattered exchange: o_recv
+    [N, T, P, Hs, 512] and lse_recv [N, T, P, Hs] as delivered by the
+    all-to-all; parts p < hist_parts of every source plus (if local_src >= 0)
+    part hist_parts of source local_src.  Returns o_latent [T, Hs, 512] and
+    lse [T, Hs]."""
+    N, T, P, Hs, _ = o_recv.shape
+    _need(o_recv, "o_recv")
+    _need(lse_recv, "lse_recv")
+    out_dtype = out_dtype or o_recv.dtype
+    if o_latent is None:
+        o_latent = torch.empty((T, Hs, D_LATENT), dtype=out_dtype, device=o_recv.device)
+    if lse_out is None:
+        lse_out = torch.empty((T, Hs), dtype=torch.float32, device=o_recv.device)
+    st = _ffi.lib().mla_dcp_combine_exchanged(
+        _p(o_recv), _p(lse_recv), N, P, int(hist_parts), int(local_src), T, Hs,
+        _code(o_recv.dtype), _code(o_latent.dtype), _p(o_latent), _p(lse_out), _s(stream))
+    _ffi.check("mla_dcp_combine_exchanged", st)
+    return o_latent, lse_out
 
 
 def mla_dcp_decode_partial_noalloc(q_abs, q_pe, kv_cache, block_table, seq_lens,

@@ -152,17 +152,18 @@ int check_partial_args(const void* q_abs, const void* q_pe, const void* kv_cache
 
 extern "C" {
 
-int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_cache,
-                           const int32_t* block_table, const int32_t* seq_lens,
-                           const void* kv_cur, int B, int q_len, int H, int num_blocks,
-                           int block_size, int max_blocks, int num_shards, float scale,
-                           int in_dtype, int part_dtype, void* o_part, float* lse_part,
-                           int32_t* err_flag, void* workspace, uint64_t workspace_bytes,
-                           mla_stream_t stream) {
+int mla_dcp_decode_partial_sliced(const void* q_abs, const void* q_pe, const void* kv_cache,
+                                  const int32_t* block_table, const int32_t* seq_lens,
+                                  const void* kv_cur, int B, int q_len, int H, int num_blocks,
+                                  int block_size, int max_blocks, int num_shards, float scale,
+                                  int in_dtype, int part_dtype, void* o_part, float* lse_part,
+                                  int32_t* err_flag, void* workspace, uint64_t workspace_bytes,
+                                  int head_slices, mla_stream_t stream) {
   const int rc = check_partial_args(q_abs, q_pe, kv_cache, block_table, seq_lens, kv_cur, B,
                                     q_len, H, num_blocks, block_size, max_blocks, num_shards,
                                     scale, in_dtype, part_dtype, o_part, lse_part);
   if (rc != MLA_OK) return rc;
+  if (head_slices < 1 || H % head_slices != 0) return MLA_ERR_BAD_SHAPE;
   if (workspace && reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return MLA_ERR_MISALIGNED;
 
   const bool bf16 = in_dtype == MLA_BF16;
@@ -202,6 +203,8 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
   pp.has_cur = kv_cur ? 1 : 0;
   pp.P = num_shards + pp.has_cur;
   pp.num_units = B * q_len * pp.P;   // checked above to fit an int
+  pp.T = B * q_len;
+  pp.head_slices = head_slices;
   pp.box_rows = box_k;
   pp.box_rows_v = box_v;
   pp.scale_log2 = scale * 1.4426950408889634f;
@@ -225,6 +228,19 @@ int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_c
   }
   return launched(mla::launch_partial(tm_qlat, tm_qpe, tm_kv, tm_cur, tm_kv_v, tm_cur_v, pp, bf16,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_cache,
+                           const int32_t* block_table, const int32_t* seq_lens,
+                           const void* kv_cur, int B, int q_len, int H, int num_blocks,
+                           int block_size, int max_blocks, int num_shards, float scale,
+                           int in_dtype, int part_dtype, void* o_part, float* lse_part,
+                           int32_t* err_flag, void* workspace, uint64_t workspace_bytes,
+                           mla_stream_t stream) {
+  return mla_dcp_decode_partial_sliced(q_abs, q_pe, kv_cache, block_table, seq_lens, kv_cur, B,
+                                       q_len, H, num_blocks, block_size, max_blocks, num_shards,
+                                       scale, in_dtype, part_dtype, o_part, lse_part, err_flag,
+                                       workspace, workspace_bytes, 1, stream);
 }
 
 uint64_t mla_dcp_decode_partial_workspace_size(int B, int q_len, int num_shards, int has_current) {
@@ -329,6 +345,28 @@ int mla_lse_combine(const void* o_part, const float* lse_part, int num_parts, co
   return launched(mla::launch_combine(o_part, lse_part, num_parts, o_local, lse_local, T, H,
                                       part_dtype, out_dtype, o_latent, lse_out,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mla_dcp_combine_exchanged(const void* o_recv, const float* lse_recv, int num_src,
+                              int parts_per_src, int hist_parts, int local_src, int T, int H,
+                              int part_dtype, int out_dtype, void* o_latent, float* lse_out,
+                              mla_stream_t stream) {
+  if (!o_recv || !lse_recv || !o_latent) return MLA_ERR_NULL_POINTER;
+  if (!is_part_dtype(part_dtype) || !is_part_dtype(out_dtype)) return MLA_ERR_BAD_DTYPE;
+  if (T < 1 || H < 1 || H > MLA_MAX_HEADS || num_src < 1) return MLA_ERR_BAD_SHAPE;
+  if (static_cast<int64_t>(num_src) * T * parts_per_src * H > INT32_MAX / 2)
+    return MLA_ERR_BAD_SHAPE;
+  if (parts_per_src < 1 || parts_per_src > MLA_MAX_SHARDS + 1 || hist_parts < 0 ||
+      hist_parts > parts_per_src || local_src < -1 || local_src >= num_src ||
+      (local_src >= 0 && hist_parts >= parts_per_src))
+    return MLA_ERR_BAD_SHARDS;
+  const int64_t np = static_cast<int64_t>(num_src) * hist_parts + (local_src >= 0 ? 1 : 0);
+  if (np < 1 || np > 96) return MLA_ERR_BAD_SHARDS;
+  if (!aligned16(o_recv) || !aligned16(o_latent)) return MLA_ERR_MISALIGNED;
+  return launched(mla::launch_combine_exchanged(o_recv, lse_recv, num_src, parts_per_src,
+                                                hist_parts, local_src, T, H, part_dtype,
+                                                out_dtype, o_latent, lse_out,
+                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
 static int vup_common(bool combine, const void* o_part, const float* lse_part, int num_parts,

@@ -197,6 +197,80 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const void* o_part, co
   if (lse_out && lane == 0) lse_out[row] = lse[0];
 }
 
+// ---------------------------------------------------------------- combine of exchanged partials
+// Decode context parallelism across GPUs (vllm-ascend PR #16977 study page,
+// the third change: the all-to-all of history partials with heads scattered,
+// then the combine of all shards plus the local partial exactly once).  After
+// a head-scattered all-to-all every rank holds, for its slice of H heads,
+// the partials of all nsrc ranks as [nsrc][T][P][H] rows.  Parts
+// (src, p < hist) are every rank's history shards; the CURRENT partial
+// (part hist, computed by every rank alike) is taken once, from source
+// local_src.  One warp per (t, h) row, lane l owns elements [16l, 16l + 16).
+template <bool F32>
+__global__ void __launch_bounds__(256) mla_combine_exchanged_kernel(
+    const void* o_recv, const float* lse_recv, int nsrc, int P, int hist, int local_src, int T,
+    int H, int part_dt, int out_dt, void* o_latent, float* lse_out) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= static_cast<int64_t>(T) * H) return;
+  const int64_t t = row / H;
+  const int h = static_cast<int>(row % H);
+  const int nh = nsrc * hist;
+  const int np = nh + (local_src >= 0 ? 1 : 0);
+  auto part_row = [&](int q) -> int64_t {
+    const int src = q < nh ? q / hist : local_src;
+    const int p = q < nh ? q - src * hist : hist;
+    return ((static_cast<int64_t>(src) * T + t) * P + p) * H + h;
+  };
+  // weights: lane l holds parts l, l + 32, l + 64 (np <= 96, checked by the host)
+  float v[3];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const int q = lane + 32 * k;
+    v[k] = q < np ? __ldg(lse_recv + part_row(q)) : -INFINITY;
+    mx = fmaxf(mx, v[k]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    v[k] = (mx == -INFINITY || v[k] == -INFINITY) ? 0.f : __expf(v[k] - mx);
+    sum += v[k];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  RowWeights rw;
+#pragma unroll
+  for (int k = 0; k < 3; ++k) rw.w[k] = v[k] * inv;
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  constexpr int KB = F32 ? 4 : 8;   // parts per batch of loads
+  for (int q0 = 0; q0 < np; q0 += KB) {
+    Chunk16<F32> x[KB];
+    float w[KB];
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+      const int q = q0 + k;
+      w[k] = q < np ? weight_of(rw, q) : 0.f;
+      if (w[k] != 0.f) {
+        x[k] = load16<F32>(o_recv, part_row(q) * 512 + lane * 16);
+      } else {
+#pragma unroll
+        for (int i = 0; i < (F32 ? 4 : 2); ++i) x[k].v[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < KB; ++k)
+      if (w[k] != 0.f) fma16<F32>(x[k], part_dt, w[k], acc);
+  }
+  store16(o_latent, row * 512 + lane * 16, acc, out_dt);
+  if (lse_out && lane == 0) lse_out[row] = sum > 0.f ? mx + __logf(sum) : -INFINITY;
+}
+
 // ---------------------------------------------------------------- V-up
 constexpr int kVupRows = 64;                    // rows (N) per MMA tile
 constexpr int kVupWBytes = 512 * 128 * 2;       // W_UV[h]: 128 KB
@@ -687,6 +761,20 @@ int launch_combine(const void* o_part, const float* lse_part, int P, const void*
   else
     mla_combine_kernel<false><<<blocks, 256, 0, stream>>>(o_part, lse_part, P, o_local, lse_local,
                                                           T, H, part_dt, out_dt, o_latent, lse_out);
+  return 0;
+}
+
+int launch_combine_exchanged(const void* o_recv, const float* lse_recv, int nsrc, int P,
+                             int hist, int local_src, int T, int H, int part_dt, int out_dt,
+                             void* o_latent, float* lse_out, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(T) * H;
+  const int blocks = static_cast<int>((rows + 7) / 8);
+  if (part_dt == kFP32)
+    mla_combine_exchanged_kernel<true><<<blocks, 256, 0, stream>>>(
+        o_recv, lse_recv, nsrc, P, hist, local_src, T, H, part_dt, out_dt, o_latent, lse_out);
+  else
+    mla_combine_exchanged_kernel<false><<<blocks, 256, 0, stream>>>(
+        o_recv, lse_recv, nsrc, P, hist, local_src, T, H, part_dt, out_dt, o_latent, lse_out);
   return 0;
 }
 

@@ -14,6 +14,8 @@ struct PartialParams {
   float* lse_part;
   int* err;
   int B, q_len, H, num_blocks, bs, max_blocks, S, P, has_cur;
+  int T;                 // B * q_len query tokens
+  int head_slices;       // o_part / lse_part as [head_slices][T][P][H / head_slices]
   int num_units;
   int box_rows;          // rows per TMA box of the QK CTA's KV maps: min(128, block_size)
   int box_rows_v;        // rows per TMA box of the PV CTA's KV maps: min(64, block_size)
@@ -50,6 +52,11 @@ constexpr int kPartialBoxV = 64;
 int launch_partial(const CUtensorMap& qlat, const CUtensorMap& qpe, const CUtensorMap& kv,
                    const CUtensorMap& cur, const CUtensorMap& kv_v, const CUtensorMap& cur_v,
                    const PartialParams& pp, bool bf16, cudaStream_t stream);
+// Combine of partials received from an all-to-all: parts (src, p < hist)
+// of [nsrc][T][P][H] rows, then part hist of source local_src (if >= 0).
+int launch_combine_exchanged(const void* o_recv, const float* lse_recv, int nsrc, int P,
+                             int hist, int local_src, int T, int H, int part_dt, int out_dt,
+                             void* o_latent, float* lse_out, cudaStream_t stream);
 int launch_combine(const void* o_part, const float* lse_part, int P, const void* o_local,
                    const float* lse_local, int T, int H, int part_dt, int out_dt, void* o_latent,
                    float* lse_out, cudaStream_t stream);

@@ -90,6 +90,17 @@ __device__ __forceinline__ UnitInfo unit_info(const PartialParams& pp, int u) {
   return ui;
 }
 
+// Row of o_part / lse_part holding token t (= b * q_len + i), part p, head h.
+// The partials are laid out as head_slices blocks of H / head_slices heads,
+// [head_slices][T][P][H / head_slices]; with one slice that is [T][P][H].
+// (Slices make each destination's share of a head-scattered all-to-all one
+// contiguous block.)
+__device__ __forceinline__ int64_t part_row(const PartialParams& pp, int64_t t, int p, int h) {
+  const int hs = pp.H / pp.head_slices;
+  const int s = h / hs;
+  return ((static_cast<int64_t>(s) * pp.T + t) * pp.P + p) * hs + (h - s * hs);
+}
+
 // Tile range of one cluster: tiles [j_begin, ...) of unit u_begin through
 // tiles [..., j_stop) of unit u_last, in the flat order of the units' tiles
 // (global tile index t_begin of the first one).
@@ -622,8 +633,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       for (int u = cid; u < pp.num_units; u += ncl) {
         const UnitInfo ui = unit_info<TILE>(pp, u);
         if (ui.ntiles != 0) continue;
-        const int64_t row0 = (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H;
-        for (int h = t; h < pp.H; h += 64) pp.lse_part[row0 + h] = -INFINITY;
+        const int64_t tok = static_cast<int64_t>(ui.b) * pp.q_len + ui.i;
+        for (int h = t; h < pp.H; h += 64) pp.lse_part[part_row(pp, tok, ui.p, h)] = -INFINITY;
       }
     } else {
       // ------------------------------------------------ rank 0: softmax
@@ -905,9 +916,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       for (int u = cid; u < pp.num_units; u += ncl) {
         const UnitInfo ui = unit_info<TILE>(pp, u);
         if (ui.ntiles != 0) continue;
-        const int64_t row0 = (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H;
+        const int64_t tok = static_cast<int64_t>(ui.b) * pp.q_len + ui.i;
         for (int h = 0; h < pp.H; ++h) {
-          const int64_t e0 = (row0 + h) * 512;
+          const int64_t e0 = part_row(pp, tok, ui.p, h) * 512;
           if (pp.part_dtype == kFP32) {
             float4* o = reinterpret_cast<float4*>(static_cast<float*>(pp.o_part) + e0);
             for (int c = lane; c < 128; c += 32) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -981,7 +992,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           tc_fence_after();
           const float lse2 = m2 + __log2f(lsum);          // log2 domain
           const int64_t row_out =
-              (static_cast<int64_t>(ui.b * pp.q_len + ui.i) * pp.P + ui.p) * pp.H + r;
+              part_row(pp, static_cast<int64_t>(ui.b) * pp.q_len + ui.i, ui.p, r);   // r < H only
           const float inv_l = 1.f / lsum;
           if (it.whole()) {
             // two TMEM loads in flight per wait
@@ -1152,7 +1163,7 @@ __global__ void __launch_bounds__(256) mla_partial_merge_kernel(PartialParams pp
         }
       }
     }
-    const int64_t row = static_cast<int64_t>(u) * pp.H + r;
+    const int64_t row = part_row(pp, u / pp.P, u % pp.P, r);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t v[32];

@@ -384,6 +384,47 @@ def test_workspace_too_small_is_rejected():
     assert e.value.status == 2
 
 
+# ------------------------------------------------------------------ decode context parallelism
+@pytest.mark.parametrize("world", [2, 4])
+def test_dcp_kernels_with_the_exchange_done_by_hand(world):
+    """The GPU steps of a DCP decode step across `world` ranks, with the
+    all-to-all done by hand on one GPU: each rank's sliced partials over its
+    piece of the history (the sliced layout must be the plain one with heads
+    regrouped, bit for bit), block r of every rank stacked (what rank r
+    receives), then mla_dcp_combine_exchanged and mla_vup with rank r's
+    heads: equal to one softmax over the whole sequence for those heads."""
+    import dataclasses
+    from mla_decode_attention_kv_gb300 import dcp
+    cfg = inputs.DecodeConfig(name="dcpg", batch=3, heads=128, q_len=2, num_shards=2,
+                              block_size=32, ragged=(1, 700), current=True, seed=311)
+    prob = inputs.make_problem(cfg)
+    T, P, hs = cfg.batch * cfg.q_len, cfg.num_shards + 1, cfg.heads // world
+    sends = []
+    for r in range(world):
+        table, lens = dcp.local_block_table(prob.block_table, prob.seq_lens, cfg.block_size,
+                                            world, r)
+        dp = DeviceProblem(dataclasses.replace(prob, block_table=table, seq_lens=lens))
+        o_s, l_s = dp.partial(head_slices=world)
+        o_p, l_p = dp.partial()
+        torch.cuda.synchronize()
+        assert dp.err.item() == 0
+        assert torch.equal(o_s, o_p.reshape(T, P, world, hs, 512).permute(2, 0, 1, 3, 4))
+        assert torch.equal(l_s, l_p.reshape(T, P, world, hs).permute(2, 0, 1, 3))
+        sends.append((o_s, l_s))
+    W = DeviceProblem(prob).W
+    for r in range(world):
+        o_recv = torch.stack([s[0][r] for s in sends]).contiguous()
+        l_recv = torch.stack([s[1][r] for s in sends]).contiguous()
+        o_lat, lse = api.mla_dcp_combine_exchanged(o_recv, l_recv, hist_parts=cfg.num_shards,
+                                                   local_src=r, out_dtype=W.dtype)
+        out = api.mla_vup(o_lat, W[r * hs:(r + 1) * hs].contiguous())
+        torch.cuda.synchronize()
+        ref_o, ref_l, ref_out = om.decode_reference(prob, heads=range(r * hs, (r + 1) * hs))
+        assert_out_close(f64(o_lat).reshape(ref_o.shape), ref_o, f"o_latent rank {r}")
+        assert_lse_close(f64(lse).reshape(ref_l.shape), ref_l, f"lse rank {r}")
+        assert_out_close(f64(out), ref_out, f"out rank {r}")
+
+
 # ------------------------------------------------------------------ streams and errors
 def test_user_stream_no_implicit_sync():
     dp = DeviceProblem(inputs.make_problem(SMALL["ragged_bf16_cur"]))
