@@ -27,7 +27,10 @@ W_UV           [H, 512, 128]               per-head V up-projection
 =============  ==========================  =====================================
 
 Recipe: ``numpy.random.default_rng(seed)``; values are N(0, 1) * 0.1 drawn in
-float32 and rounded to nearest-even in the storage dtype.  Draw order:
+float32 and rounded to nearest-even in the storage dtype.  An FP8 latent
+cache (``kv_dtype="e4m3"``) stores the cache and CURRENT values divided by
+``kv_scale`` (a power of two) as E4M3 bytes, rounded to nearest-even and
+saturated at +-448; q and W_UV keep the model dtype.  Draw order:
 (ragged history lengths), q_abs, q_pe, kv_cache, kv_cur, W_UV, block-table
 permutation.  The block table is a random permutation of all physical blocks
 cut per sequence (or the identity), so a sequence's pages are scattered over
@@ -63,11 +66,17 @@ class DecodeConfig:
     current: bool = False            # CURRENT segment present (kv_cur)
     dtype: str = "bf16"              # storage dtype of q, cache, W_UV
     part_dtype: str = "bf16"         # dtype of the per-shard partial outputs
+    kv_dtype: str = ""               # cache / kv_cur storage dtype ("" = dtype, or "e4m3")
+    kv_scale: float = 1.0            # e4m3 cache: value = decoded byte * kv_scale
     shuffle_table: bool = True
     equal_logit_rows: tuple = ()     # sequences whose q is all zero
     q_gain: float = 1.0              # test-only: scales q to sharpen softmax
     std: float = 0.1
     seed: int = 0
+
+    @property
+    def cache_dtype(self) -> str:
+        return self.kv_dtype or self.dtype
 
     @property
     def scale(self) -> float:
@@ -78,7 +87,7 @@ class DecodeConfig:
         return dataclasses.replace(self, **kw)
 
 
-# The five workloads that define this library's test and bench surface.
+# The workloads that define this library's test and bench surface.
 CONFIGS = {
     "tiny": DecodeConfig(
         name="tiny", batch=1, heads=16, q_len=1, num_shards=2, block_size=64,
@@ -96,6 +105,11 @@ CONFIGS = {
     "verylong": DecodeConfig(
         name="verylong", batch=16, heads=128, q_len=1, num_shards=16,
         block_size=64, history=131072),
+    # the very long context over an FP8 (E4M3) latent cache, kv_scale 2^-8
+    # (stored values ~ N(0, 25.6): no saturation at 448)
+    "verylong_fp8": DecodeConfig(
+        name="verylong_fp8", batch=16, heads=128, q_len=1, num_shards=16,
+        block_size=64, history=131072, kv_dtype="e4m3", kv_scale=2.0 ** -8),
 }
 
 
@@ -123,8 +137,32 @@ class DecodeProblem:
         return self.cfg.num_shards + (1 if self.kv_cur is not None else 0)
 
 
+def _e4m3_positive_values() -> np.ndarray:
+    """Values of the E4M3 codes 0x00..0x7E (sign 0, 4 exponent bits with bias
+    7, 3 mantissa bits; exponent field 0 is subnormal; 0x7F is NaN)."""
+    codes = np.arange(0x7F)
+    e, m = codes >> 3, codes & 7
+    return np.where(e == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * 2.0 ** (e - 7.0))
+
+
+def _round_e4m3(x: np.ndarray) -> np.ndarray:
+    """float -> E4M3 bytes: nearest representable value, ties to the even
+    code (mantissa LSB 0), magnitudes above 448 saturate to 448."""
+    vals = _e4m3_positive_values()
+    a = np.minimum(np.abs(np.asarray(x, dtype=np.float64)), vals[-1])
+    hi = np.clip(np.searchsorted(vals, a, side="left"), 0, len(vals) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - vals[lo], vals[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(a == vals[hi], hi, np.where(pick_hi, hi, lo)).astype(np.uint8)
+    sign = (np.signbit(np.asarray(x, dtype=np.float64)) & (code != 0)).astype(np.uint8)
+    return code | (sign << np.uint8(7))
+
+
 def round_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
     """float32 -> storage bits, round to nearest even."""
+    if dtype == "e4m3":
+        return _round_e4m3(x)
     x = np.ascontiguousarray(x, dtype=np.float32)
     if dtype == "fp16":
         return x.astype(np.float16).view(np.uint16)
@@ -137,7 +175,7 @@ def round_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
 
 def _normal_bits(rng, shape, std, dtype, gain=1.0) -> np.ndarray:
     n = int(np.prod(shape))
-    out = np.empty(n, dtype=np.uint16)
+    out = np.empty(n, dtype=np.uint8 if dtype == "e4m3" else np.uint16)
     for lo in range(0, n, _CHUNK):
         hi = min(n, lo + _CHUNK)
         v = rng.standard_normal(hi - lo, dtype=np.float32)
@@ -173,8 +211,10 @@ def make_problem(cfg: DecodeConfig, seq_lens: Optional[np.ndarray] = None
 
     blocks_per_seq = [(int(L) + bs - 1) // bs for L in lens]
     num_blocks = max(1, sum(blocks_per_seq))
-    kv_cache = _normal_bits(rng, (num_blocks, bs, D_QK), cfg.std, cfg.dtype)
-    kv_cur = (_normal_bits(rng, (B, q, D_QK), cfg.std, cfg.dtype)
+    # an e4m3 cache stores value / kv_scale
+    kv_gain = 1.0 / cfg.kv_scale if cfg.cache_dtype == "e4m3" else 1.0
+    kv_cache = _normal_bits(rng, (num_blocks, bs, D_QK), cfg.std, cfg.cache_dtype, kv_gain)
+    kv_cur = (_normal_bits(rng, (B, q, D_QK), cfg.std, cfg.cache_dtype, kv_gain)
               if cfg.current else None)
     W_UV = _normal_bits(rng, (H, D_LATENT, D_V), cfg.std, cfg.dtype)
 
@@ -195,4 +235,4 @@ def kv_bytes(problem: DecodeProblem) -> int:
     """Bytes of latent KV one decode step must read (history + current)."""
     cur = problem.cfg.q_len if problem.kv_cur is not None else 0
     tokens = int(problem.seq_lens.astype(np.int64).sum()) + problem.cfg.batch * cur
-    return tokens * D_QK * 2
+    return tokens * D_QK * (1 if problem.cfg.cache_dtype == "e4m3" else 2)

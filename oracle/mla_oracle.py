@@ -48,6 +48,14 @@ Readings where the pages are silent: natural-log LSE; scale 1/sqrt(192)
 (the 128 + 64 head width of the explicit form); fp32-width LSE outputs;
 all-empty rows give o = 0 and lse = -inf.
 
+FP8 latent cache (a variant the pages only point towards: the compressed KV
+direction of the Kthena x Mooncake page, sections 3.2 and 5.2).  The plain
+reading taken: every cached value (history and CURRENT, latent and RoPE) is
+one E4M3 byte e times one per-tensor scale kv_scale; the attention itself is
+unchanged and runs on the decoded values e * kv_scale.  E4M3 is the OCP FP8
+format: sign bit, 4 exponent bits with bias 7, 3 mantissa bits, exponent
+field 0 subnormal, no infinities, 0x7F / 0xFF NaN.
+
 Every function below is pinned by tests that do not reuse its arithmetic:
 brute force on tiny inputs, the explicitly materialised per-head form, a
 library attention routine, sharded-versus-unsharded equality and closed-form
@@ -67,8 +75,22 @@ D_V = 128           # per-head V width after V-up   ([PR] code block A)
 
 
 # ---------------------------------------------------------------- decoding
+def e4m3_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact float64 value of E4M3 bytes, from the format's definition:
+    (-1)^s * 2^(e-7) * (1 + m/8) for e > 0, (-1)^s * 2^-6 * (m/8) for e = 0,
+    NaN for e = 15, m = 7."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    s = np.where(b >> 7, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 7).astype(np.float64)
+    mag = np.where(e == 0, 2.0 ** -6 * (m / 8.0), np.ldexp(1.0 + m / 8.0, e - 7))
+    return np.where((e == 15) & (m == 7), np.nan, s * mag)
+
+
 def to_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
-    """Exact float64 value of raw bf16 / fp16 storage bits."""
+    """Exact float64 value of raw bf16 / fp16 / E4M3 storage bits."""
+    if dtype == "e4m3":
+        return e4m3_to_f64(bits)
     bits = np.asarray(bits, dtype=np.uint16)
     if dtype == "fp16":
         return bits.view(np.float16).astype(np.float64)
@@ -145,17 +167,25 @@ def _queries(problem, b, i, heads):
     return q_abs, q_pe
 
 
+def cache_values(bits, cfg):
+    """Values of cached tokens: the storage bits decoded, times kv_scale for
+    an E4M3 cache."""
+    if cfg.cache_dtype == "e4m3":
+        return e4m3_to_f64(bits) * cfg.kv_scale
+    return to_f64(bits, cfg.cache_dtype)
+
+
 def _history(problem, b):
     L = int(problem.seq_lens[b])
     bits = gather_history_fast(problem.kv_cache, problem.block_table[b],
                                problem.cfg.block_size, L)
-    return to_f64(bits, problem.cfg.dtype)
+    return cache_values(bits, problem.cfg)
 
 
 def _current(problem, b):
     if problem.kv_cur is None:
         return np.zeros((0, D_QK))
-    return to_f64(problem.kv_cur[b], problem.cfg.dtype)
+    return cache_values(problem.kv_cur[b], problem.cfg)
 
 
 def _all_heads(problem):

@@ -70,6 +70,91 @@ def test_bits_decode_exact():
     assert om.to_f64(np.array([0x3C00], np.uint16), "fp16")[0] == 1.0
 
 
+# ----------------------------------------------------------------- E4M3 cache
+def test_e4m3_decode_special_codes():
+    """Codes whose values follow directly from the E4M3 definition (bias 7,
+    3 mantissa bits, subnormals at exponent field 0, 0x7F / 0xFF NaN)."""
+    cases = {0x00: 0.0, 0x38: 1.0, 0xB8: -1.0, 0x40: 2.0, 0x3C: 1.5, 0x7E: 448.0,
+             0xFE: -448.0, 0x08: 2.0 ** -6, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9,
+             0x77: 240.0, 0x30: 0.5, 0x28: 0.25}
+    got = om.e4m3_to_f64(np.array(list(cases), dtype=np.uint8))
+    assert np.array_equal(got, np.array(list(cases.values())))
+    neg0 = om.e4m3_to_f64(np.array([0x80], np.uint8))[0]
+    assert neg0 == 0.0 and np.signbit(neg0)
+    assert np.all(np.isnan(om.e4m3_to_f64(np.array([0x7F, 0xFF], np.uint8))))
+
+
+def test_e4m3_decode_equals_torch_float8():
+    """All 256 codes against torch's float8_e4m3fn conversion (a separate
+    implementation of the same format)."""
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = om.e4m3_to_f64(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+def test_e4m3_codes_monotone_and_spaced():
+    """Positive codes 0x00..0x7E increase; the step up from code c is the ulp
+    2^(e-10) of c's binade e (exponent field; the subnormal step 2^-9 equals
+    the first normal binade's)."""
+    v = om.e4m3_to_f64(np.arange(0x7F, dtype=np.uint8))
+    d = np.diff(v)
+    assert np.all(d > 0)
+    e = np.maximum(np.arange(0, 0x7E) >> 3, 1)
+    assert np.array_equal(d, np.ldexp(1.0, e - 10))
+
+
+def test_e4m3_generator_rounds_to_nearest_even():
+    """The input generator's E4M3 rounding, by brute force over all codes:
+    the nearest finite value, ties to the even code, saturation at 448."""
+    vals = om.e4m3_to_f64(np.arange(0x7F, dtype=np.uint8))
+    x = np.concatenate([RNG.standard_normal(4000) * 30, RNG.standard_normal(2000) * 0.01,
+                        (vals[1:] + vals[:-1]) / 2, vals, [500.0, -1e6, 464.0]])
+    codes = inputs.round_to_bits(x.astype(np.float32), "e4m3")
+    got = om.e4m3_to_f64(codes)
+    xf = x.astype(np.float32).astype(np.float64)
+    a = np.minimum(np.abs(xf), 448.0)
+    dist = np.abs(a[:, None] - vals[None, :])
+    best = dist.min(axis=1)
+    assert np.all(np.abs(np.abs(got) - a) == best)
+    ties = (dist == best[:, None]).sum(axis=1) == 2
+    assert np.all((codes[ties] & 1) == 0)
+    nz = got != 0
+    assert np.all(np.sign(got[nz]) == np.sign(xf[nz]))
+
+
+def test_e4m3_cache_attention_equals_decoded_16bit_cache():
+    """An E4M3 problem attends over byte * kv_scale: the same problem with the
+    cache stored as those exact values in bf16 (every E4M3 value times a power
+    of two is a bf16 value), decoded by torch, gives identical results."""
+    torch = pytest.importorskip("torch")
+    cfg = inputs.DecodeConfig(name="f8", batch=2, heads=4, q_len=2, num_shards=2, block_size=16,
+                              ragged=(3, 90), current=True, kv_dtype="e4m3", kv_scale=2.0 ** -7,
+                              seed=41)
+    p8 = inputs.make_problem(cfg)
+
+    def as_bf16(bits):
+        v = torch.from_numpy(bits).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        v = v * cfg.kv_scale
+        out = inputs.round_to_bits(v.astype(np.float32), "bf16")
+        assert np.array_equal(om.to_f64(out, "bf16"), v)
+        return out
+
+    import dataclasses
+    p16 = dataclasses.replace(p8, cfg=cfg.with_(kv_dtype=""), kv_cache=as_bf16(p8.kv_cache),
+                              kv_cur=as_bf16(p8.kv_cur))
+    o8, l8, y8 = om.decode_reference(p8)
+    o16, l16, y16 = om.decode_reference(p16)
+    assert np.array_equal(o8, o16) and np.array_equal(l8, l16) and np.array_equal(y8, y16)
+    a8, b8 = om.decode_partials(p8)
+    a16, b16 = om.decode_partials(p16)
+    assert np.array_equal(a8, a16) and np.array_equal(b8, b16)
+
+
 # ----------------------------------------------------------------- gather
 def test_gather_tags_through_shuffled_table():
     cfg = inputs.DecodeConfig(name="g", batch=3, heads=2, q_len=1,
@@ -385,6 +470,8 @@ def _pins_pass():
         test_sharded_combine_equals_single_softmax(2)
         test_vup_identity_blocks_and_head_order()
         test_combine_random_boundaries_and_empty_shards()
+        test_e4m3_decode_equals_torch_float8()
+        test_e4m3_cache_attention_equals_decoded_16bit_cache()
     except AssertionError:
         return False
     return True
@@ -396,9 +483,25 @@ def test_pins_pass_unmodified():
 
 @pytest.mark.parametrize("mutant", ["drop_rope", "rope_sign", "scale_sqrt128",
                                     "transposed_wuv", "combine_no_weights",
-                                    "lse_log2"])
+                                    "lse_log2", "e4m3_bias8", "e4m3_no_subnormals",
+                                    "kv_scale_dropped"])
 def test_planted_mistake_is_caught(monkeypatch, mutant):
     real_seg, real_comb, real_vup = om.segment_attention, om.lse_combine, om.v_up
+    real_e4m3, real_cache = om.e4m3_to_f64, om.cache_values
+
+    def e4m3(bits):
+        v = real_e4m3(bits)
+        b = np.asarray(bits, dtype=np.uint8)
+        if mutant == "e4m3_bias8":
+            v = v / 2.0
+        if mutant == "e4m3_no_subnormals":
+            v = np.where((b & 0x78) == 0, 0.0, v)
+        return v
+
+    def cache(bits, cfg):
+        if mutant == "kv_scale_dropped" and cfg.cache_dtype == "e4m3":
+            return om.e4m3_to_f64(bits)
+        return real_cache(bits, cfg)
 
     def seg(q_abs, q_pe, tokens, scale, visible=None):
         if mutant == "drop_rope":
@@ -426,4 +529,6 @@ def test_planted_mistake_is_caught(monkeypatch, mutant):
     monkeypatch.setattr(om, "segment_attention", seg)
     monkeypatch.setattr(om, "lse_combine", comb)
     monkeypatch.setattr(om, "v_up", vup)
+    monkeypatch.setattr(om, "e4m3_to_f64", e4m3)
+    monkeypatch.setattr(om, "cache_values", cache)
     assert not _pins_pass()
