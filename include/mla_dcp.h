@@ -6,6 +6,7 @@
  *
  *   mla_dcp_decode_partial  per-shard (and CURRENT-chunk) partial attention
  *                           outputs and their log-sum-exp
+ *   mla_dcp_decode_partial_fp8  the same over an FP8 (E4M3) latent cache
  *   mla_lse_combine         LSE-weighted merge of the partials: the result
  *                           equals one softmax over the whole sequence
  *   mla_vup                 per-head V up-projection, latent 512 -> 128
@@ -17,6 +18,8 @@
  *         (huashanblogllm.xyz study-dcp-decode-streams-vup)
  *   [TP]  MLA multi-GPU TP configuration article (hncyxsy.com news 238223)
  *   [K3]  "RTPLLM推理优化：K3芯片上MLA注意力的DCP与通算融合实践" (zwxr.cn 254603)
+ *   [KM]  the Kthena x Mooncake KV-cache reuse article (its KV compression
+ *         sections 3.2 and 5.2)
  *
  * Conventions shared by every call
  *   - All tensor pointers are DEVICE pointers owned by the caller; the
@@ -110,7 +113,9 @@ enum {
  * Arguments
  *   q_abs      [B, q_len, H, 512] in_dtype  query absorbed into latent space
  *   q_pe       [B, q_len, H, 64]  in_dtype  RoPE query, already rotated
- *   kv_cache   [num_blocks, block_size, 576] in_dtype
+ *   kv_cache   [num_blocks, block_size, 576] in_dtype.  The slots of a
+ *              sequence's last block past L_b are read with the block (and
+ *              weighted by 0), so they must hold finite values.
  *   block_table[B, max_blocks] int32   physical block ids; entries past
  *              ceil(L_b / block_size) are never read
  *   seq_lens   [B] int32 (device)  history lengths, 0 <= L_b <= max_blocks*block_size;
@@ -165,6 +170,39 @@ int mla_dcp_decode_partial_sliced(const void* q_abs, const void* q_pe, const voi
                                   int in_dtype, int part_dtype, void* o_part, float* lse_part,
                                   int32_t* err_flag, void* workspace, uint64_t workspace_bytes,
                                   int head_slices, mla_stream_t stream);
+
+/*
+ * mla_dcp_decode_partial_fp8 -- mla_dcp_decode_partial_sliced over an FP8
+ * latent cache.
+ *
+ * Defines: the KV compression direction of [KM] (sections 3.2 and 5.2),
+ * which the sources only point towards; the format is this library's
+ * reading: every cached value, history and CURRENT, latent and RoPE, is one
+ * E4M3 byte e (OCP FP8: bias 7, 3 mantissa bits, no infinities, 0x7F / 0xFF
+ * NaN) times one per-tensor kv_scale, so that c_t and kR_t above are the
+ * decoded bytes times kv_scale.  The results are those of
+ * mla_dcp_decode_partial on those values.
+ *
+ * Differences from mla_dcp_decode_partial_sliced:
+ *   kv_cache   [num_blocks, block_size, 576] bytes (E4M3); slots of a last
+ *              block past L_b may hold any bytes
+ *   kv_cur     [B, q_len, 576] bytes (E4M3, the same kv_scale), or NULL
+ *   kv_scale   > 0 and finite (scale * kv_scale too); MLA_ERR_BAD_SHAPE otherwise
+ * Precision: the tensor cores multiply the cache bytes by the query in two
+ * E4M3 terms (a power-of-two row scale, then the rounded row and its rounded
+ * remainder), which keeps |error of q| <= 2^-8 |q| + 2^-17 max|q row|,
+ * about the precision of bf16; P is rounded to fp16.  The cache must not
+ * hold the NaN codes in visible slots.  Every other argument, result and
+ * error (including the workspace, of the same size) as
+ * mla_dcp_decode_partial_sliced.
+ */
+int mla_dcp_decode_partial_fp8(const void* q_abs, const void* q_pe, const void* kv_cache,
+                               const int32_t* block_table, const int32_t* seq_lens,
+                               const void* kv_cur, int B, int q_len, int H, int num_blocks,
+                               int block_size, int max_blocks, int num_shards, float scale,
+                               float kv_scale, int in_dtype, int part_dtype, void* o_part,
+                               float* lse_part, int32_t* err_flag, void* workspace,
+                               uint64_t workspace_bytes, int head_slices, mla_stream_t stream);
 
 /*
  * mla_dcp_decode_partial_workspace_size -- bytes of workspace that

@@ -24,6 +24,8 @@ SIGNATURES = {
                                    ctypes.c_uint64, P]),
     "mla_dcp_decode_partial_sliced": (I, [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, P, P,
                                           P, ctypes.c_uint64, I, P]),
+    "mla_dcp_decode_partial_fp8": (I, [P, P, P, P, P, P, I, I, I, I, I, I, I, F, F, I, I, P, P,
+                                       P, P, ctypes.c_uint64, I, P]),
     "mla_dcp_decode_partial_workspace_size": (ctypes.c_uint64, [I, I, I, I]),
     "mla_dcp_combine_exchanged": (I, [P, P, I, I, I, I, I, I, I, I, P, P, P]),
     "mla_dcp_decode_partial_noalloc": (I, [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, P, P,

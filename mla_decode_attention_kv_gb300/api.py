@@ -69,15 +69,22 @@ def partial_workspace(device, B: int, q_len: int, num_shards: int, has_current: 
     return ws
 
 
+def is_fp8_cache(kv_cache) -> bool:
+    """An E4M3 cache: uint8 bytes or torch.float8_e4m3fn."""
+    return kv_cache.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8))
+
+
 def mla_dcp_decode_partial(q_abs, q_pe, kv_cache, block_table, seq_lens, num_shards: int, *,
                            kv_cur=None, scale: float = DEFAULT_SCALE, part_dtype=None,
                            o_part=None, lse_part=None, err_flag=None, stream=None,
-                           workspace="default", head_slices: int = 1):
+                           workspace="default", head_slices: int = 1, kv_scale=None):
     """Partial attention of every (sequence, query token, shard [, CURRENT]).
 
     q_abs [B, q, H, 512], q_pe [B, q, H, 64], kv_cache [num_blocks, bs, 576],
     block_table [B, max_blocks] int32, seq_lens [B] int32 (history lengths),
-    kv_cur [B, q, 576] or None.  Returns o_part [B, q, P, H, 512] and
+    kv_cur [B, q, 576] or None.  A kv_cache of E4M3 bytes (torch.uint8 or
+    torch.float8_e4m3fn; kv_cur likewise) goes to mla_dcp_decode_partial_fp8
+    with kv_scale (default 1.0).  Returns o_part [B, q, P, H, 512] and
     lse_part [B, q, P, H] (float32), P = num_shards + (kv_cur is not None);
     with head_slices = N > 1 they are [N, B*q, P, H/N, 512] and
     [N, B*q, P, H/N] (mla_dcp_decode_partial_sliced: block n is what rank n
@@ -109,6 +116,19 @@ def mla_dcp_decode_partial(q_abs, q_pe, kv_cache, block_table, seq_lens, num_sha
         workspace = partial_workspace(q_abs.device, B, q_len, num_shards, kv_cur is not None,
                                       stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if is_fp8_cache(kv_cache):
+        if kv_cur is not None and not is_fp8_cache(kv_cur):
+            raise TypeError("kv_cur must be E4M3 bytes like kv_cache")
+        st = _ffi.lib().mla_dcp_decode_partial_fp8(
+            _p(q_abs), _p(q_pe), _p(kv_cache), _p(block_table), _p(seq_lens), _p(kv_cur),
+            B, q_len, H, num_blocks, bs, block_table.shape[1], num_shards, float(scale),
+            float(1.0 if kv_scale is None else kv_scale), _code(q_abs.dtype),
+            _code(o_part.dtype), _p(o_part), _p(lse_part), _p(err_flag), _p(workspace), ws_bytes,
+            int(head_slices), _s(stream))
+        _ffi.check("mla_dcp_decode_partial_fp8", st)
+        return o_part, lse_part
+    if kv_scale is not None:
+        raise TypeError("kv_scale applies to an E4M3 cache only")
     st = _ffi.lib().mla_dcp_decode_partial_sliced(
         _p(q_abs), _p(q_pe), _p(kv_cache), _p(block_table), _p(seq_lens), _p(kv_cur),
         B, q_len, H, num_blocks, bs, block_table.shape[1], num_shards, float(scale),
@@ -235,13 +255,14 @@ def mla_gather_kv(kv_cache, block_table, seq_lens, max_len: int, *, dst=None, er
 
 def decode_step(q_abs, q_pe, kv_cache, block_table, seq_lens, W_UV, num_shards: int, *,
                 kv_cur=None, scale: float = DEFAULT_SCALE, part_dtype=None, o_part=None,
-                lse_part=None, out=None, err_flag=None, stream=None, workspace="default"):
+                lse_part=None, out=None, err_flag=None, stream=None, workspace="default",
+                kv_scale=None):
     """One decode step of the attention layer: partials, then the fused
     combine + V-up.  Returns out [B*q, H*128]."""
     o_part, lse_part = mla_dcp_decode_partial(
         q_abs, q_pe, kv_cache, block_table, seq_lens, num_shards, kv_cur=kv_cur, scale=scale,
         part_dtype=part_dtype, o_part=o_part, lse_part=lse_part, err_flag=err_flag,
-        stream=stream, workspace=workspace)
+        stream=stream, workspace=workspace, kv_scale=kv_scale)
     return mla_lse_combine_vup(o_part, lse_part, W_UV, out=out, err_flag=err_flag, stream=stream)
 
 

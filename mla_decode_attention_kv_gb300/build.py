@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB_PATH = os.path.join(HERE, "libmla_dcp.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "partial.cu", "combine_vup.cu", "gather.cu"]
+SOURCES = ["api.cu", "partial.cu", "partial_fp8.cu", "combine_vup.cu", "gather.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I" + INCLUDE]

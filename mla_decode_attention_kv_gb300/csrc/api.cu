@@ -63,6 +63,21 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over a row-major [rows, cols] byte tensor (E4M3 values), 128-byte
+// swizzle; the part of a box past `cols` is zero-filled.
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                 uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool is_half_dtype(int d) { return d == MLA_BF16 || d == MLA_FP16; }
 bool is_part_dtype(int d) { return d == MLA_BF16 || d == MLA_FP16 || d == MLA_FP32; }
@@ -150,19 +165,22 @@ int check_partial_args(const void* q_abs, const void* q_pe, const void* kv_cache
 }
 }  // namespace
 
-extern "C" {
-
-int mla_dcp_decode_partial_sliced(const void* q_abs, const void* q_pe, const void* kv_cache,
-                                  const int32_t* block_table, const int32_t* seq_lens,
-                                  const void* kv_cur, int B, int q_len, int H, int num_blocks,
-                                  int block_size, int max_blocks, int num_shards, float scale,
-                                  int in_dtype, int part_dtype, void* o_part, float* lse_part,
-                                  int32_t* err_flag, void* workspace, uint64_t workspace_bytes,
-                                  int head_slices, mla_stream_t stream) {
+namespace {
+// The partial call over a 16-bit cache (kv8 false: kv values in in_dtype) or
+// an E4M3 cache (kv8 true: one byte per value, times kv_scale).
+int decode_partial(bool kv8, const void* q_abs, const void* q_pe, const void* kv_cache,
+                   const int32_t* block_table, const int32_t* seq_lens, const void* kv_cur, int B,
+                   int q_len, int H, int num_blocks, int block_size, int max_blocks,
+                   int num_shards, float scale, float kv_scale, int in_dtype, int part_dtype,
+                   void* o_part, float* lse_part, int32_t* err_flag, void* workspace,
+                   uint64_t workspace_bytes, int head_slices, mla_stream_t stream) {
   const int rc = check_partial_args(q_abs, q_pe, kv_cache, block_table, seq_lens, kv_cur, B,
                                     q_len, H, num_blocks, block_size, max_blocks, num_shards,
                                     scale, in_dtype, part_dtype, o_part, lse_part);
   if (rc != MLA_OK) return rc;
+  if (kv8 && (!(kv_scale > 0.f) || !std::isfinite(kv_scale) ||
+              !std::isfinite(scale * kv_scale * 1.4426950408889634f)))
+    return MLA_ERR_BAD_SHAPE;
   if (head_slices < 1 || H % head_slices != 0) return MLA_ERR_BAD_SHAPE;
   if (workspace && reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return MLA_ERR_MISALIGNED;
 
@@ -171,18 +189,26 @@ int mla_dcp_decode_partial_sliced(const void* q_abs, const void* q_pe, const voi
   const int box_v = block_size < mla::kPartialBoxV ? block_size : mla::kPartialBoxV;
   const uint64_t qrows = static_cast<uint64_t>(B) * q_len * H;
   const uint64_t kv_rows = static_cast<uint64_t>(num_blocks) * block_size;
+  const uint64_t cur_rows = static_cast<uint64_t>(B) * q_len;
   CUtensorMap tm_qlat, tm_qpe, tm_kv, tm_cur, tm_kv_v, tm_cur_v;
   if (!make_map(&tm_qlat, q_abs, 512, qrows, 1024, 64, 128, bf16) ||
-      !make_map(&tm_qpe, q_pe, 64, qrows, 128, 64, 128, bf16) ||
-      !make_map(&tm_kv, kv_cache, 576, kv_rows, 1152, 64, box_k, bf16) ||
-      !make_map(&tm_kv_v, kv_cache, 576, kv_rows, 1152, 64, box_v, bf16))
+      !make_map(&tm_qpe, q_pe, 64, qrows, 128, 64, 128, bf16))
     return MLA_ERR_CUDA;
-  if (kv_cur) {
-    const uint64_t cur_rows = static_cast<uint64_t>(B) * q_len;
-    if (!make_map(&tm_cur, kv_cur, 576, cur_rows, 1152, 64, box_k, bf16) ||
-        !make_map(&tm_cur_v, kv_cur, 576, cur_rows, 1152, 64, box_v, bf16))
+  if (kv8) {
+    // 576-byte token rows in 128-byte boxes
+    if (!make_map_u8(&tm_kv, kv_cache, 576, kv_rows, 576, 128, box_k) ||
+        !make_map_u8(&tm_kv_v, kv_cache, 576, kv_rows, 576, 128, box_v) ||
+        (kv_cur && (!make_map_u8(&tm_cur, kv_cur, 576, cur_rows, 576, 128, box_k) ||
+                    !make_map_u8(&tm_cur_v, kv_cur, 576, cur_rows, 576, 128, box_v))))
       return MLA_ERR_CUDA;
   } else {
+    if (!make_map(&tm_kv, kv_cache, 576, kv_rows, 1152, 64, box_k, bf16) ||
+        !make_map(&tm_kv_v, kv_cache, 576, kv_rows, 1152, 64, box_v, bf16) ||
+        (kv_cur && (!make_map(&tm_cur, kv_cur, 576, cur_rows, 1152, 64, box_k, bf16) ||
+                    !make_map(&tm_cur_v, kv_cur, 576, cur_rows, 1152, 64, box_v, bf16))))
+      return MLA_ERR_CUDA;
+  }
+  if (!kv_cur) {
     tm_cur = tm_kv;     // never read
     tm_cur_v = tm_kv_v;
   }
@@ -207,7 +233,8 @@ int mla_dcp_decode_partial_sliced(const void* q_abs, const void* q_pe, const voi
   pp.head_slices = head_slices;
   pp.box_rows = box_k;
   pp.box_rows_v = box_v;
-  pp.scale_log2 = scale * 1.4426950408889634f;
+  pp.scale_log2 = scale * (kv8 ? kv_scale : 1.f) * 1.4426950408889634f;
+  pp.out_scale = kv8 ? kv_scale : 1.f;
   pp.spin_limit = mla::partial_spin_limit();
   pp.part_dtype = part_dtype;
   pp.split = 0;
@@ -226,8 +253,40 @@ int mla_dcp_decode_partial_sliced(const void* q_abs, const void* q_pe, const voi
     pp.ws_lse = reinterpret_cast<float*>(w + recs);
     pp.ws_o = w + recs + 2 * static_cast<size_t>(clusters) * 128 * 4;
   }
-  return launched(mla::launch_partial(tm_qlat, tm_qpe, tm_kv, tm_cur, tm_kv_v, tm_cur_v, pp, bf16,
-                                      reinterpret_cast<cudaStream_t>(stream)));
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return launched(kv8 ? mla::launch_partial_fp8(tm_qlat, tm_qpe, tm_kv, tm_cur, tm_kv_v, tm_cur_v,
+                                                pp, bf16, st)
+                      : mla::launch_partial(tm_qlat, tm_qpe, tm_kv, tm_cur, tm_kv_v, tm_cur_v, pp,
+                                            bf16, st));
+}
+}  // namespace
+
+extern "C" {
+
+int mla_dcp_decode_partial_sliced(const void* q_abs, const void* q_pe, const void* kv_cache,
+                                  const int32_t* block_table, const int32_t* seq_lens,
+                                  const void* kv_cur, int B, int q_len, int H, int num_blocks,
+                                  int block_size, int max_blocks, int num_shards, float scale,
+                                  int in_dtype, int part_dtype, void* o_part, float* lse_part,
+                                  int32_t* err_flag, void* workspace, uint64_t workspace_bytes,
+                                  int head_slices, mla_stream_t stream) {
+  return decode_partial(false, q_abs, q_pe, kv_cache, block_table, seq_lens, kv_cur, B, q_len, H,
+                        num_blocks, block_size, max_blocks, num_shards, scale, 1.f, in_dtype,
+                        part_dtype, o_part, lse_part, err_flag, workspace, workspace_bytes,
+                        head_slices, stream);
+}
+
+int mla_dcp_decode_partial_fp8(const void* q_abs, const void* q_pe, const void* kv_cache,
+                               const int32_t* block_table, const int32_t* seq_lens,
+                               const void* kv_cur, int B, int q_len, int H, int num_blocks,
+                               int block_size, int max_blocks, int num_shards, float scale,
+                               float kv_scale, int in_dtype, int part_dtype, void* o_part,
+                               float* lse_part, int32_t* err_flag, void* workspace,
+                               uint64_t workspace_bytes, int head_slices, mla_stream_t stream) {
+  return decode_partial(true, q_abs, q_pe, kv_cache, block_table, seq_lens, kv_cur, B, q_len, H,
+                        num_blocks, block_size, max_blocks, num_shards, scale, kv_scale, in_dtype,
+                        part_dtype, o_part, lse_part, err_flag, workspace, workspace_bytes,
+                        head_slices, stream);
 }
 
 int mla_dcp_decode_partial(const void* q_abs, const void* q_pe, const void* kv_cache,

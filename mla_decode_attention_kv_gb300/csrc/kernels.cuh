@@ -19,7 +19,8 @@ struct PartialParams {
   int num_units;
   int box_rows;          // rows per TMA box of the QK CTA's KV maps: min(128, block_size)
   int box_rows_v;        // rows per TMA box of the PV CTA's KV maps: min(64, block_size)
-  float scale_log2;      // softmax scale * log2(e)
+  float scale_log2;      // softmax scale * log2(e) (times kv_scale for an E4M3 cache)
+  float out_scale;       // E4M3 cache: kv_scale, applied to O in the epilogue
   uint32_t spin_limit;   // polls before a pipeline wait gives up (MLA_DEV_WAIT_TIMEOUT)
   int part_dtype;        // 0 bf16, 1 fp16, 2 fp32
   // Split-unit workspace (split = number of CTA pairs, 0 = whole units):
@@ -52,6 +53,13 @@ constexpr int kPartialBoxV = 64;
 int launch_partial(const CUtensorMap& qlat, const CUtensorMap& qpe, const CUtensorMap& kv,
                    const CUtensorMap& cur, const CUtensorMap& kv_v, const CUtensorMap& cur_v,
                    const PartialParams& pp, bool bf16, cudaStream_t stream);
+// The partial kernel over an E4M3 cache: kv / cur maps of 128-byte boxes
+// (min(128, block_size) rows), kv_v / cur_v of 128-byte boxes of
+// min(64, block_size) rows; qlat / qpe as for the 16-bit kernel.
+int launch_partial_fp8(const CUtensorMap& qlat, const CUtensorMap& qpe, const CUtensorMap& kv,
+                       const CUtensorMap& cur, const CUtensorMap& kv_v, const CUtensorMap& cur_v,
+                       const PartialParams& pp, bool bf16, cudaStream_t stream);
+int partial_fp8_max_clusters();
 // Combine of partials received from an all-to-all: parts (src, p < hist)
 // of [nsrc][T][P][H] rows, then part hist of source local_src (if >= 0).
 int launch_combine_exchanged(const void* o_recv, const float* lse_recv, int nsrc, int P,

@@ -42,134 +42,10 @@
 //           w3 zeros of empty parts, w4-7 O rescale + epilogue (thread = row)
 // Every wait is bounded; on timeout the kernel records MLA_DEV_WAIT_TIMEOUT,
 // raises an abort flag, drains its own copies and MMAs, frees TMEM, returns.
-#include <climits>
 #include <mutex>
-#include "common.cuh"
-#include "kernels.cuh"
+#include "partial_sched.cuh"
 
 namespace mla {
-
-// Token range of one unit.  History shard p of sequence b covers
-// [p*len, min(L, (p+1)*len)), len = bs * ceil(L / (S*bs)) (block-aligned,
-// trailing shards possibly empty).  The CURRENT part covers kv_cur[b, 0..i].
-// Units are numbered u = ((b * q_len + i) * P + p), so the parts of one query
-// token are consecutive and a cluster walking a contiguous range reuses Q.
-struct UnitInfo {
-  int b, i, p;
-  int lo, hi;
-  bool current;
-  int ntiles;
-};
-
-template <int TILE>
-__device__ __forceinline__ UnitInfo unit_info(const PartialParams& pp, int u) {
-  UnitInfo ui;
-  ui.p = u % pp.P;
-  const int bi = u / pp.P;
-  ui.i = bi % pp.q_len;
-  ui.b = bi / pp.q_len;
-  ui.current = pp.has_cur && ui.p == pp.S;
-  if (ui.current) {
-    ui.lo = 0;
-    ui.hi = ui.i + 1;
-  } else {
-    int L = pp.seq_lens[ui.b];
-    const int cap = pp.max_blocks * pp.bs;
-    if (L < 0 || L > cap) {
-      // a history longer than its block-table row (or negative): flagged,
-      // then clamped so that no access leaves the table
-      set_error(pp.err, kDevBadSeqLen);
-      L = max(0, min(L, cap));
-    }
-    const int chunk = pp.S * pp.bs;
-    const int len = L > 0 ? pp.bs * ((L + chunk - 1) / chunk) : 0;
-    ui.lo = min(L, ui.p * len);
-    ui.hi = min(L, (ui.p + 1) * len);
-  }
-  ui.ntiles = (ui.hi - ui.lo + TILE - 1) / TILE;
-  return ui;
-}
-
-// Row of o_part / lse_part holding token t (= b * q_len + i), part p, head h.
-// The partials are laid out as head_slices blocks of H / head_slices heads,
-// [head_slices][T][P][H / head_slices]; with one slice that is [T][P][H].
-// (Slices make each destination's share of a head-scattered all-to-all one
-// contiguous block.)
-__device__ __forceinline__ int64_t part_row(const PartialParams& pp, int64_t t, int p, int h) {
-  const int hs = pp.H / pp.head_slices;
-  const int s = h / hs;
-  return ((static_cast<int64_t>(s) * pp.T + t) * pp.P + p) * hs + (h - s * hs);
-}
-
-// Tile range of one cluster: tiles [j_begin, ...) of unit u_begin through
-// tiles [..., j_stop) of unit u_last, in the flat order of the units' tiles
-// (global tile index t_begin of the first one).
-struct TileRange {
-  int u_begin, j_begin, u_last, j_stop, t_begin;
-};
-
-// Walks the tiles of a TileRange as one flat stream.  A "piece" is the part
-// of one unit inside the range: the whole unit, or (at the ends of the range
-// of a cluster that splits units) a run of its tiles.
-template <int TILE>
-struct TileIter {
-  int u, j, k, nq, qkey;
-  int jfirst, jend;      // tile bounds of the current piece within its unit
-  int ustart;            // global tile index of the unit's first tile
-  int u_last, j_stop;
-  bool newq, valid;
-  UnitInfo ui;
-  __device__ __forceinline__ void start(const PartialParams& pp, const TileRange& r) {
-    u_last = r.u_last;
-    j_stop = r.j_stop;
-    k = -1;
-    nq = -1;
-    qkey = -1;
-    valid = r.u_begin <= r.u_last;
-    if (!valid) return;
-    u = r.u_begin;
-    ui = unit_info<TILE>(pp, u);
-    ustart = r.t_begin - r.j_begin;
-    enter(pp, r.j_begin);
-  }
-  __device__ __forceinline__ void enter(const PartialParams& pp, int j0) {
-    ++k;
-    j = jfirst = j0;
-    jend = u == u_last ? j_stop : ui.ntiles;
-    const int key = ui.b * pp.q_len + ui.i;
-    newq = key != qkey;
-    if (newq) {
-      ++nq;
-      qkey = key;
-    }
-  }
-  __device__ __forceinline__ void next_unit(const PartialParams& pp) {
-    while (u < u_last) {
-      ustart += ui.ntiles;
-      ++u;
-      ui = unit_info<TILE>(pp, u);
-      if (ui.ntiles > 0) {
-        enter(pp, 0);
-        return;
-      }
-    }
-    valid = false;
-  }
-  __device__ __forceinline__ void advance(const PartialParams& pp) {
-    if (++j >= jend) next_unit(pp);
-  }
-  __device__ __forceinline__ bool first() const { return j == jfirst; }
-  __device__ __forceinline__ bool last() const { return j == jend - 1; }
-  // Whether the current piece is the whole unit (no other cluster holds tiles of it).
-  __device__ __forceinline__ bool whole() const { return jfirst == 0 && jend == ui.ntiles; }
-  // Whether this tile is the last one that reads the current Q.
-  __device__ __forceinline__ bool last_of_q(const PartialParams& pp) const {
-    if (!last()) return false;
-    TileIter n = *this;
-    n.next_unit(pp);
-    return !n.valid || n.newq;
-  }
-};
 
 // Shared-memory plan (offsets from a 1024-aligned base; same size on both
 // ranks).  Rank 0: K ring, Q RoPE tile, one outgoing P message.
@@ -329,166 +205,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Tile share of this cluster: tiles [lo, hi) of the flat order of all
-  // units' tiles, lo = cid * T / ncl.  With a workspace the share is exact
-  // and the units at its ends may be split with the neighbouring clusters
-  // (their pieces are merged through the workspace); without one the cluster
-  // owns the whole units whose first tile falls in its share.  Units without
-  // tiles (o = 0, lse = -inf) are dealt round-robin: unit u to cluster
-  // u mod clusters, so a batch of short or empty histories spreads its zero
-  // rows over every pair.  Both CTAs of the pair compute the same range.
+  // Tile share of this pair (partition_tiles); units without tiles are
+  // dealt round-robin: unit u to pair u mod pairs, so a batch of short or
+  // empty histories spreads its zero rows over every pair.
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(nclusters_x());
-  __shared__ int s_scan[8];
-  __shared__ int s_load[256];
-  __shared__ int s_rng[4];
   TileRange rng;
-  int64_t share_total = 0;
+  Shares shares;
   bool split = false;
-  // share of pair c: tiles [share_start(c), share_start(c + 1))
-  auto share_start = [&](int c) -> int64_t { return static_cast<int64_t>(c) * share_total / ncl; };
-  auto cluster_of = [&](int64_t t) -> int {   // the pair whose share holds tile t
-    int c = static_cast<int>(t * ncl / share_total);
-    while (c + 1 < ncl && share_start(c + 1) <= t) ++c;
-    while (c > 0 && share_start(c) > t) --c;
-    return c;
-  };
-  auto holds = [&](int c) { return share_start(c + 1) > share_start(c); };
-  {
-    const int U = pp.num_units;
-    const int per = (U + 255) / 256;
-    const int a = min(U, static_cast<int>(threadIdx.x) * per);
-    const int e = min(U, a + per);
-    int cnt = 0;
-    for (int u = a; u < e; ++u) cnt += unit_info<TILE>(pp, u).ntiles;
-    // exclusive block scan of cnt: warp inclusive scans, then the warp totals
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) s_scan[warp] = incl;   // warp totals (s_scan reused below)
-    if (threadIdx.x == 0) {
-      s_rng[0] = INT_MAX;   // u_begin
-      s_rng[1] = 0;         // j_begin
-      s_rng[2] = -1;        // u_last
-      s_rng[3] = 0;         // j_stop
-    }
-    for (int c = threadIdx.x; c < ncl; c += 256) s_load[c] = 0;
-    __syncthreads();
-    int warp_base = 0, all = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      const int t = s_scan[w];
-      warp_base += w < warp ? t : 0;
-      all += t;
-    }
-    const int my_start = warp_base + incl - cnt;   // tiles before this thread's units
-    share_total = all;
-    if (pp.split && share_total > 0) {
-      // Split units only where whole units would leave the busiest pair above
-      // the even share by more than max(2 tiles, 1/8 of the share): the
-      // merge kernel and the extra unit ends cost about that much.
-      int64_t run = my_start;
-      for (int u = a; u < e; ++u) {
-        const int nt = unit_info<TILE>(pp, u).ntiles;
-        if (nt > 0) atomicAdd(&s_load[cluster_of(run)], nt);
-        run += nt;
-      }
-      __syncthreads();
-      int mx = 0;
-      for (int c = threadIdx.x; c < ncl; c += 256) mx = max(mx, s_load[c]);
-      const int64_t even = (share_total + ncl - 1) / ncl;
-      // any pair above the threshold decides for all
-      split = __syncthreads_or(mx > even + max(int64_t{2}, even / 8)) != 0;
-    }
-    const int64_t lo = share_start(cid);
-    const int64_t hi = share_start(cid + 1);
-    int64_t run = my_start;
-    for (int u = a; u < e; ++u) {
-      const int nt = unit_info<TILE>(pp, u).ntiles;
-      if (nt > 0 && lo < hi) {
-        if (split) {
-          if (lo >= run && lo < run + nt) {
-            s_rng[0] = u;
-            s_rng[1] = static_cast<int>(lo - run);
-          }
-          if (hi - 1 >= run && hi - 1 < run + nt) {
-            s_rng[2] = u;
-            s_rng[3] = static_cast<int>(hi - run);
-          }
-        } else if (run >= lo && run < hi) {
-          atomicMin(&s_rng[0], u);
-          atomicMax(&s_rng[2], u);
-        }
-      }
-      run += nt;
-    }
-    __syncthreads();
-    rng.u_begin = s_rng[0];
-    rng.j_begin = s_rng[1];
-    rng.u_last = s_rng[2];
-    rng.j_stop = split ? s_rng[3] : (rng.u_last >= 0 ? unit_info<TILE>(pp, rng.u_last).ntiles : 0);
-    rng.t_begin = static_cast<int>(lo);
-  }
+  partition_tiles<TILE>(pp, cid, ncl, rng, shares, split);
 
-  // Protocol waits give up after pp.spin_limit polls (the drains at the end
-  // of the kernel, which wait for copies and MMAs already issued, use the
-  // fixed kSpinLimit: those always complete).
-  const uint32_t spin_limit = pp.spin_limit;
-  auto wait = [&](uint64_t* b, uint32_t parity) -> bool {
-    for (uint32_t it = 0; it < spin_limit; ++it) {
-      if (mbar_try_wait(b, parity)) return true;
-      if ((it & 1023u) == 1023u && *abort_flag) return false;
-    }
-    set_error(err, kDevWaitTimeout);
-    *abort_flag = 1;
-    return false;
-  };
-  // Waits of whole warp groups off the issue path: polls may suspend.
-  auto wait_lazy = [&](uint64_t* b, uint32_t parity) -> bool {
-    for (uint32_t it = 0; it < spin_limit; ++it) {
-      if (mbar_try_wait_sleep(b, parity, kLazyWaitNs)) return true;
-      if ((it & 15u) == 15u && *abort_flag) return false;
-    }
-    set_error(err, kDevWaitTimeout);
-    *abort_flag = 1;
-    return false;
-  };
-  auto wait_cl = [&](uint64_t* b, uint32_t parity) -> bool {
-    for (uint32_t it = 0; it < spin_limit; ++it) {
-      if (mbar_try_wait_cluster(b, parity)) return true;
-      if ((it & 1023u) == 1023u && *abort_flag) return false;
-    }
-    set_error(err, kDevWaitTimeout);
-    *abort_flag = 1;
-    return false;
-  };
-  // TMA box `l` (of `br` rows) of the tile starting at token t0 of the unit.
-  // Box rows of a tile, one box per lane.  fetch_id only issues the
-  // block-table load of the lane's box (one tile ahead); box_row, called when
-  // that tile is issued, checks the id and forms the row, so the producer
-  // never waits on a table load.  Boxes past the unit's end re-read its last
-  // box (in bounds, masked out by the softmax).
+  const Waits waits{pp.spin_limit, abort_flag, err};
+  auto wait = [&](uint64_t* b, uint32_t parity) { return waits.wait(b, parity); };
+  auto wait_lazy = [&](uint64_t* b, uint32_t parity) { return waits.lazy(b, parity); };
+  auto wait_cl = [&](uint64_t* b, uint32_t parity) { return waits.cluster(b, parity); };
   const int bs_shift = __ffs(pp.bs) - 1;   // block sizes are powers of two
-  auto fetch_id = [&](const TileIter<TILE>& t, int br, int l) -> int {
-    if (!t.valid || t.ui.current) return 0;
-    const int tk = min(t.ui.lo + t.j * TILE + l * br, t.ui.hi - 1);
-    return __ldg(pp.block_table + static_cast<int64_t>(t.ui.b) * pp.max_blocks + (tk >> bs_shift));
+  auto fetch_id = [&](const TileIter<TILE>& t, int br, int l) {
+    return mla::fetch_id<TILE>(pp, t, br, l, bs_shift);
   };
-  auto box_row = [&](const TileIter<TILE>& t, int br, int l, int id) -> int {
-    if (t.ui.current) return t.ui.b * pp.q_len + l * br;
-    int tk = t.ui.lo + t.j * TILE + l * br;
-    const bool past = tk >= t.ui.hi;
-    if (past) tk = t.ui.hi - 1;
-    if (id < 0 || id >= pp.num_blocks) {
-      set_error(err, kDevBadBlockId);
-      id = 0;
-    }
-    int row = (id << bs_shift) + (tk & (pp.bs - 1));
-    if (past) row &= ~(br - 1);
-    return row;
+  auto box_row = [&](const TileIter<TILE>& t, int br, int l, int id) {
+    return mla::box_row<TILE>(pp, t, br, l, id, bs_shift);
   };
   const int br_k = pp.box_rows;           // rank 0 box rows: min(128, bs)
   const int br_v = pp.box_rows_v;         // rank 1 box rows: min(32, bs)
@@ -1043,21 +779,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   tmem_wait_ld();
   tc_fence_before();
   __syncthreads();
-  if (pp.split && rank == 1 && threadIdx.x == 0) {
-    // Record the split unit whose last tile this pair holds (if any) for the
-    // merge kernel: the unit at the start of the share, cut before it and
-    // ending inside it.  Written on every call with a workspace.
-    int4 rec = make_int4(-1, 0, 0, 0);
-    if (split && rng.u_begin <= rng.u_last && rng.j_begin > 0) {
-      const int nt = unit_info<TILE>(pp, rng.u_begin).ntiles;
-      if (rng.u_begin < rng.u_last || rng.j_stop == nt) {
-        const int64_t ustart = share_start(cid) - rng.j_begin;
-        rec = make_int4(rng.u_begin, static_cast<int>(ustart), cluster_of(ustart), cid);
-      }
-    }
-    pp.ws_units[cid] = rec;
-    if (cid == 0) pp.ws_units[ncl] = make_int4(static_cast<int>(share_total), ncl, 0, 0);
-  }
+  if (pp.split && rank == 1 && threadIdx.x == 0) record_split_unit<TILE>(pp, cid, rng, shares, split);
   cluster_sync();
   if (rank == 1 && threadIdx.x == 64) {
     // Drain the P messages rank 0 sent that the PV issuer never saw land
@@ -1087,11 +809,10 @@ __global__ void __launch_bounds__(256) mla_partial_merge_kernel(PartialParams pp
   const int u = rec.x;
   if (u < 0) return;
   const int4 hdr = pp.ws_units[gridDim.x];
-  const int64_t total = hdr.x;
-  const int ncl = hdr.y;
+  const Shares sh{hdr.x, hdr.y};
   const int64_t ustart = rec.y;
   const int c_first = rec.z, c_last = rec.w;
-  auto share_start = [&](int c) -> int64_t { return static_cast<int64_t>(c) * total / ncl; };
+  auto share_start = [&](int c) { return sh.start(c); };
   __shared__ int s_slot[256];
   __shared__ float s_w[256 * 32];       // per candidate pair, per row of the pass: weight
   __shared__ float s_lsetot[32];
@@ -1214,10 +935,14 @@ static int prepare_partial(int* clusters) {
   return 0;
 }
 
+// Pairs that every partial kernel (16-bit and E4M3 caches) can hold at once:
+// the workspace is sized for this many.
 int partial_max_clusters() {
   int a = 0, b = 0;
   if (prepare_partial<true>(&a) != 0 || prepare_partial<false>(&b) != 0) return -1;
-  return std::min(a, b);
+  const int c = partial_fp8_max_clusters();
+  if (c < 1) return -1;
+  return std::min(std::min(a, b), c);
 }
 
 template <bool BF16>
@@ -1232,22 +957,23 @@ static int launch_partial_t(const CUtensorMap& qlat, const CUtensorMap& qpe, con
   if (clusters > max_clusters) return -1;
   mla_partial_kernel<BF16><<<dim3(2 * clusters), dim3(256), PairSmem::kTotal, stream>>>(
       qlat, qpe, kv, cur, kv_v, cur_v, pp);
-  if (pp.split) {
-    // programmatic dependent launch: the merge grid is scheduled while the
-    // partial grid drains and waits for it on the device (griddepcontrol)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(clusters, 2, 1);
-    cfg.blockDim = dim3(256, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, mla_partial_merge_kernel, pp) != cudaSuccess) return -1;
-  }
-  return 0;
+  return pp.split ? launch_partial_merge(pp, clusters, stream) : 0;
+}
+
+// Programmatic dependent launch: the merge grid is scheduled while the
+// partial grid drains and waits for it on the device (griddepcontrol).
+int launch_partial_merge(const PartialParams& pp, int clusters, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clusters, 2, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_partial_merge_kernel, pp) != cudaSuccess ? -1 : 0;
 }
 
 int launch_partial(const CUtensorMap& qlat, const CUtensorMap& qpe, const CUtensorMap& kv,

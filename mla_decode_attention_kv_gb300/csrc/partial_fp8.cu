@@ -1,0 +1,983 @@
+// Partial attention per context shard over an FP8 (E4M3) latent cache:
+// mla_dcp_decode_partial_fp8.
+//
+// Every cached value (latent c_KV and RoPE key k_R, history and CURRENT) is
+// one E4M3 byte times a per-tensor kv_scale; the attention is the one of the
+// 16-bit kernel (partial.cu) on those values.  The work units, the tile
+// shares of the CTA pairs, the split-role pair and its P-message protocol are
+// the same; what changes is how each CTA feeds its tensor cores:
+//
+//   rank 0 (QK CTA): a K tile is 128 tokens x 576 bytes, moved by TMA as five
+//     128-byte chunks (four latent, one RoPE chunk whose upper 64 bytes are the
+//     zero fill of an out-of-range box) straight into kind::f8f6f4 MMAs
+//     (E4M3 x E4M3, fp32 accumulate).  The 16-bit query row is turned into
+//     E4M3 once per query token with a power-of-two row scale sq and two
+//     terms, q = sq * (hi + lo) + e with hi = rn(q / sq), lo = rn(q / sq - hi):
+//     |e| <= 2^-8 |q| + 2^-17 max|q_row|, about the precision of bf16.  S is
+//     accumulated as Q_hi K^T + Q_lo K^T (two MMAs per k-step: the tensor
+//     work of the 16-bit kernel, on half the bytes).
+//   rank 1 (PV CTA): V stages of E4M3 bytes are widened to fp16 in shared
+//     memory by the four epilogue warps (exact: every E4M3 value is an fp16
+//     value), then O += P V as kind::f16 MMAs with P in fp16.
+// kv_scale is folded into the softmax scale and into the epilogue's 1 / l.
+//
+// Warp roles (256 threads per CTA):
+//   rank 0: w0 TMA producer (query chunks, K tiles), w1 MMA issuer, w2-3 LSE
+//           of empty parts, w4-7 query quantisation + softmax (thread = row)
+//   rank 1: w0 TMA producer (E4M3 V), w1 MMA issuer, w2 hands P buffers
+//           back, w3 zeros of empty parts + P landing watcher, w4-7 V
+//           widening, O rescale and epilogue (thread = row)
+// Every wait is bounded, as in the 16-bit kernel.
+#include <cuda_fp8.h>
+#include <mutex>
+#include "partial_sched.cuh"
+
+namespace mla {
+
+namespace {
+
+// Shared-memory plan (offsets from a 1024-aligned base; same size on both ranks).
+struct Fp8Smem {
+  static constexpr int kTile = 128;
+  static constexpr int kChunk = kTile * 128;         // 128 rows x 128 bytes (16 KB)
+  static constexpr int kKPer = 5;                    // chunks per K stage: 4 latent + RoPE
+  static constexpr int kKStage = kKPer * kChunk;     // 80 KB: one tile per ring phase
+  static constexpr int kNK = 2;
+  static constexpr int kQStages = 2;                 // a query's 9 16-bit chunks: 5 + 4
+  static constexpr int kV8Sub = 64;                  // tokens per E4M3 V stage
+  static constexpr int kV8Chunk = kV8Sub * 128;      // 128 latent bytes x 64 tokens (8 KB)
+  static constexpr int kV8Stage = 4 * kV8Chunk;      // 32 KB
+  static constexpr int kNV8 = 2;
+  static constexpr int kV16Sub = 32;                 // tokens per fp16 V stage
+  static constexpr int kV16Chunk = kV16Sub * 128;    // 64 latent x 32 tokens, fp16 (4 KB)
+  static constexpr int kV16Stage = 8 * kV16Chunk;    // 32 KB
+  static constexpr int kNV16 = 2;
+  // P message: P [128 rows x 128 tokens] fp16 as two 64-token SW128 chunks,
+  // alpha[128], lsum[128], m[128], header.
+  static constexpr int kMsgP = 2 * 16384;
+  static constexpr int kMsgAlpha = kMsgP;
+  static constexpr int kMsgL = kMsgAlpha + 512;
+  static constexpr int kMsgM = kMsgL + 512;
+  static constexpr int kMsgHdr = kMsgM + 512;
+  static constexpr int kMsgBytes = kMsgHdr + 16;     // 34320, multiple of 16
+  static constexpr int kMsgStride = 34816;           // 1024-aligned slot
+  // rank 0
+  static constexpr int kKOff = 0;
+  static constexpr int kQr8Off = kKOff + kNK * kKStage;   // 163840: query RoPE, hi | lo bytes
+  static constexpr int kPsOff = kQr8Off + 16384;          // 180224: one outgoing message
+  static constexpr int kEnd0 = kPsOff + kMsgStride;       // 215040
+  // rank 1
+  static constexpr int kV8Off = 0;
+  static constexpr int kV16Off = kV8Off + kNV8 * kV8Stage;     // 65536
+  static constexpr int kPrOff = kV16Off + kNV16 * kV16Stage;   // 131072
+  static constexpr int kEnd1 = kPrOff + 2 * kMsgStride;        // 200704
+  static constexpr int kBarOff = kEnd0 > kEnd1 ? kEnd0 : kEnd1;
+  static constexpr int kTotal = kBarOff + 512 + 1024;
+};
+static_assert(Fp8Smem::kTotal <= 232448, "shared memory budget");
+static_assert(Fp8Smem::kTile == 2 * Fp8Smem::kV8Sub && Fp8Smem::kV8Sub == 2 * Fp8Smem::kV16Sub,
+              "a tile is two E4M3 V stages, each two fp16 V stages");
+
+enum : int {
+  F_KFULL = 0,
+  F_KEMPTY = F_KFULL + Fp8Smem::kNK,
+  F_Q_EMPTY = F_KEMPTY + Fp8Smem::kNK,
+  F_QLAT_FULL = F_Q_EMPTY + 1,
+  F_S_FULL = F_QLAT_FULL + 1,     // 2
+  F_S_EMPTY = F_S_FULL + 2,       // 2
+  F_PFREE = F_S_EMPTY + 2,        // 2
+  F_MMA_DONE_A = F_PFREE + 2,
+  F_MSG_FREE = F_MMA_DONE_A + 1,  // rank 0: the outgoing P message has landed in rank 1
+  F_V8FULL = F_MSG_FREE + 1,
+  F_V8EMPTY = F_V8FULL + Fp8Smem::kNV8,
+  F_V16FULL = F_V8EMPTY + Fp8Smem::kNV8,
+  F_V16EMPTY = F_V16FULL + Fp8Smem::kNV16,
+  F_P_FULL = F_V16EMPTY + Fp8Smem::kNV16,   // 2
+  F_PV_DONE = F_P_FULL + 2,       // 2
+  F_META_READ = F_PV_DONE + 2,    // 2
+  F_O_EMPTY = F_META_READ + 2,
+  F_O_FIXED = F_O_EMPTY + 1,
+  F_MMA_DONE_B = F_O_FIXED + 1,
+  F_COUNT = F_MMA_DONE_B + 1
+};
+// barriers + TMEM slot + abort flag + 4 warp flags + the P message count
+static_assert((F_COUNT + 9) * 8 <= 512, "barrier block");
+
+// Two floats -> two E4M3 bytes (round to nearest even, saturating at 448),
+// a in the low byte.
+__device__ __forceinline__ uint32_t to_e4m3x2(float a, float b) {
+  return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Two E4M3 bytes (the low one first) -> fp16x2, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t v) {
+  const uint32_t h = e4m3x2_to_f16x2(v);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// Eight 16-bit query values (one 16-byte unit), times inv_sq, as the two
+// E4M3 terms: hi[0..1] and lo[0..1] each hold 8 bytes in element order.
+template <bool BF16>
+__device__ __forceinline__ void quantize8(uint4 x, float inv_sq, uint32_t (&hi)[2],
+                                          uint32_t (&lo)[2]) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t h16[4], l16[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = unpack2(w[k], BF16 ? kBF16 : kFP16);
+    const float a = f.x * inv_sq, b = f.y * inv_sq;
+    h16[k] = to_e4m3x2(a, b);
+    const float2 d = e4m3x2_to_float2(h16[k]);
+    l16[k] = to_e4m3x2(a - d.x, b - d.y);
+  }
+  hi[0] = h16[0] | (h16[1] << 16);
+  hi[1] = h16[2] | (h16[3] << 16);
+  lo[0] = l16[0] | (l16[1] << 16);
+  lo[1] = l16[2] | (l16[3] << 16);
+}
+
+template <bool BF16>
+__device__ __forceinline__ float amax8(uint4 x, float m) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = unpack2(w[k], BF16 ? kBF16 : kFP16);
+    m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+  }
+  return m;
+}
+
+}  // namespace
+
+template <bool BF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+    mla_partial_fp8_kernel(const __grid_constant__ CUtensorMap tm_qlat,
+                           const __grid_constant__ CUtensorMap tm_qpe,
+                           const __grid_constant__ CUtensorMap tm_kv,
+                           const __grid_constant__ CUtensorMap tm_cur,
+                           const __grid_constant__ CUtensorMap tm_kv_v,
+                           const __grid_constant__ CUtensorMap tm_cur_v, const PartialParams pp) {
+  using L = Fp8Smem;
+  constexpr int TILE = L::kTile;
+  constexpr int kTmemCols = 512;
+  constexpr uint32_t kQhiCol = 0;        // rank 0: query hi bytes, 128 columns (4 per column)
+  constexpr uint32_t kQloCol = 128;      // rank 0: query lo bytes, 128 columns
+  constexpr uint32_t kSCol = 256;        // rank 0: S buffers [256,384), [384,512)
+  constexpr float kRescaleThresh = 8.0f; // lazy rescale: only when max grows by > 2^8
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + F_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + F_COUNT + 1);
+  volatile uint32_t* warp_flags = reinterpret_cast<volatile uint32_t*>(bar + F_COUNT + 2);
+  // rank 0: P messages sent; rank 1: P messages the watcher has seen land
+  volatile int* msg_count = reinterpret_cast<volatile int*>(bar + F_COUNT + 8);
+
+  const uint32_t rank = cluster_ctarank();
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  int* err = pp.err;
+
+  if (threadIdx.x == 0) {
+    if (rank == 0) {
+      for (int s = 0; s < L::kNK; ++s) {
+        mbar_init(&bar[F_KFULL + s], 1);
+        mbar_init(&bar[F_KEMPTY + s], 1);
+      }
+      mbar_init(&bar[F_Q_EMPTY], 1);
+      mbar_init(&bar[F_QLAT_FULL], 4);
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(&bar[F_S_FULL + k], 1);
+        mbar_init(&bar[F_S_EMPTY + k], 4);
+        mbar_init(&bar[F_PFREE + k], 1);
+      }
+      mbar_init(&bar[F_MMA_DONE_A], 1);
+      mbar_init(&bar[F_MSG_FREE], 1);
+    } else {
+      for (int s = 0; s < L::kNV8; ++s) {
+        mbar_init(&bar[F_V8FULL + s], 1);
+        mbar_init(&bar[F_V8EMPTY + s], 4);
+      }
+      for (int s = 0; s < L::kNV16; ++s) {
+        mbar_init(&bar[F_V16FULL + s], 4);
+        mbar_init(&bar[F_V16EMPTY + s], 1);
+      }
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(&bar[F_P_FULL + k], 1);
+        mbar_init(&bar[F_PV_DONE + k], 1);
+        mbar_init(&bar[F_META_READ + k], 4);
+      }
+      mbar_init(&bar[F_O_EMPTY], 4);
+      mbar_init(&bar[F_O_FIXED], 4);
+      mbar_init(&bar[F_MMA_DONE_B], 1);
+      // the first two P messages may land as soon as the cluster is up
+      mbar_arrive_expect_tx(&bar[F_P_FULL + 0], L::kMsgBytes);
+      mbar_arrive_expect_tx(&bar[F_P_FULL + 1], L::kMsgBytes);
+    }
+    *abort_flag = 0;
+    *msg_count = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_qlat);
+    prefetch_tmap(&tm_qpe);
+    prefetch_tmap(&tm_kv);
+    prefetch_tmap(&tm_cur);
+    prefetch_tmap(&tm_kv_v);
+    prefetch_tmap(&tm_cur_v);
+  }
+  __syncthreads();
+  cluster_sync();   // every barrier of both CTAs is initialised
+  griddep_launch_dependents();   // a dependent merge grid may be scheduled as CTAs retire
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Tile share of this pair (partition_tiles); units without tiles are dealt
+  // round-robin: unit u to pair u mod pairs.
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(nclusters_x());
+  TileRange rng;
+  Shares shares;
+  bool split = false;
+  partition_tiles<TILE>(pp, cid, ncl, rng, shares, split);
+
+  const Waits waits{pp.spin_limit, abort_flag, err};
+  auto wait = [&](uint64_t* b, uint32_t parity) { return waits.wait(b, parity); };
+  auto wait_lazy = [&](uint64_t* b, uint32_t parity) { return waits.lazy(b, parity); };
+  auto wait_cl = [&](uint64_t* b, uint32_t parity) { return waits.cluster(b, parity); };
+  const int bs_shift = __ffs(pp.bs) - 1;   // block sizes are powers of two
+  const int br_k = pp.box_rows;            // rank 0 box rows: min(128, bs)
+  const int br_v = pp.box_rows_v;          // rank 1 box rows: min(64, bs)
+
+  if (rank == 0) {
+    uint8_t* sK = smem + L::kKOff;
+    uint8_t* sQr = smem + L::kQr8Off;
+    uint8_t* sPs = smem + L::kPsOff;
+    if (warp == 0) {
+      // ------------------------------------------------ rank 0: TMA producer
+      // Converged warp: every lane polls the stage barrier, lane l issues box
+      // l of each chunk of a tile.
+      TileIter<TILE> it;
+      it.start(pp, rng);
+      int cs = 0;
+      bool ok = true;
+      const int nbox = TILE / br_k;      // boxes per chunk of a tile (1, 2, 4 or 8)
+      const bool boxlane = lane < nbox;
+      int id_cur = boxlane ? fetch_id<TILE>(pp, it, br_k, lane, bs_shift) : 0;
+      while (it.valid) {
+        const UnitInfo ui = it.ui;
+        TileIter<TILE> nx = it;
+        nx.advance(pp);
+        const int id_next = boxlane ? fetch_id<TILE>(pp, nx, br_k, lane, bs_shift) : 0;
+        if (it.first() && it.newq) {
+          // the new query's eight 64-column latent chunks and its RoPE chunk
+          // (16-bit) through the ring, 5 + 4 per stage; the softmax warps
+          // turn them into E4M3 terms
+          const int qrow = (ui.b * pp.q_len + ui.i) * pp.H;
+          for (int qs = 0; qs < L::kQStages; ++qs) {
+            const int st = cs % L::kNK;
+            if (cs >= L::kNK && !wait(&bar[F_KEMPTY + st], ((cs / L::kNK) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            const int nc = qs == 0 ? 5 : 4;
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&bar[F_KFULL + st], nc * L::kChunk);
+              for (int k = 0; k < nc; ++k) {
+                const int c = qs * 5 + k;
+                uint8_t* dst = sK + st * L::kKStage + k * L::kChunk;
+                if (c < 8)
+                  tma_load_2d(dst, &tm_qlat, &bar[F_KFULL + st], c * 64, qrow);
+                else
+                  tma_load_2d(dst, &tm_qpe, &bar[F_KFULL + st], 0, qrow);
+              }
+            }
+            ++cs;
+          }
+          if (!ok) break;
+        }
+        // K tile: five 128-byte chunks (bytes [128c, 128c + 128) of each
+        // token; chunk 4 reads bytes 512..639 of 576-byte rows, the part past
+        // the row is zero-filled)
+        const int row = boxlane ? box_row<TILE>(pp, it, br_k, lane, id_cur, bs_shift) : 0;
+        const CUtensorMap* map = ui.current ? &tm_cur : &tm_kv;
+        const int st = cs % L::kNK;
+        if (cs >= L::kNK && !wait(&bar[F_KEMPTY + st], ((cs / L::kNK) - 1) & 1)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bar[F_KFULL + st], L::kKStage);
+        if (boxlane) {
+          uint8_t* dst = sK + st * L::kKStage + lane * br_k * 128;
+#pragma unroll
+          for (int c = 0; c < L::kKPer; ++c)
+            tma_load_2d(dst + c * L::kChunk, map, &bar[F_KFULL + st], c * 128, row);
+        }
+        ++cs;
+        id_cur = id_next;
+        it = nx;
+      }
+      if (lane == 0) {
+        // drain: the last load issued into each stage has landed
+        for (int s = 0; s < L::kNK && s < cs; ++s) {
+          const int last = cs - 1 - ((cs - 1 - s) % L::kNK);
+          mbar_wait(&bar[F_KFULL + s], (last / L::kNK) & 1, err);
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------ rank 0: MMA issuer (QK)
+      if (lane == 0) {
+        // E4M3 x E4M3 -> fp32: format fields 0, both operands K-major
+        constexpr uint32_t idesc = make_idesc_f16(128, TILE, false, false, false);
+        const uint32_t k_base = smem_u32(sK);
+        const uint32_t qr_base = smem_u32(sQr);
+        TileIter<TILE> it;
+        it.start(pp, rng);
+        int g = 0, cs = 0;
+        bool ok = true;
+        while (ok && it.valid) {
+          if (it.first() && it.newq) {
+            if (!wait(&bar[F_QLAT_FULL], it.nq & 1)) break;
+            cs += L::kQStages;   // the query's ring stages are the softmax warps' to free
+          }
+          const int sb = g & 1;
+          if (g >= 2 && !wait(&bar[F_S_EMPTY + sb], ((g >> 1) - 1) & 1)) break;
+          const uint32_t d = tmem + kSCol + sb * TILE;
+          const int st = cs % L::kNK;
+          if (!wait(&bar[F_KFULL + st], (cs / L::kNK) & 1)) break;
+          tc_fence_after();
+          const uint32_t kb = k_base + st * L::kKStage;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = make_desc_sw128(kb + c * L::kChunk + kk * 32, 16, 1024);
+              umma_ts_f8(d, tmem + kQhiCol + c * 32 + kk * 8, bd, idesc, (c | kk) ? 1u : 0u);
+              umma_ts_f8(d, tmem + kQloCol + c * 32 + kk * 8, bd, idesc, 1u);
+            }
+          }
+          // RoPE: 64 bytes per row (two k-steps); the query's hi bytes are
+          // bytes 0..63 of its row, the lo bytes 64..127
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint64_t bd = make_desc_sw128(kb + 4 * L::kChunk + kk * 32, 16, 1024);
+            umma_ss_f8(d, make_desc_sw128(qr_base + kk * 32, 16, 1024), bd, idesc, 1u);
+            umma_ss_f8(d, make_desc_sw128(qr_base + 64 + kk * 32, 16, 1024), bd, idesc, 1u);
+          }
+          umma_commit(&bar[F_KEMPTY + st]);
+          ++cs;
+          umma_commit(&bar[F_S_FULL + sb]);
+          if (it.last_of_q(pp)) umma_commit(&bar[F_Q_EMPTY]);
+          it.advance(pp);
+          ++g;
+        }
+        umma_commit(&bar[F_MMA_DONE_A]);
+        mbar_wait(&bar[F_MMA_DONE_A], 0, err);
+      }
+    } else if (warp == 2 || warp == 3) {
+      // ------------------------------------------------ rank 0: LSE of empty parts
+      const int t = threadIdx.x - 64;
+      for (int u = cid; u < pp.num_units; u += ncl) {
+        const UnitInfo ui = unit_info<TILE>(pp, u);
+        if (ui.ntiles != 0) continue;
+        const int64_t tok = static_cast<int64_t>(ui.b) * pp.q_len + ui.i;
+        for (int h = t; h < pp.H; h += 64) pp.lse_part[part_row(pp, tok, ui.p, h)] = -INFINITY;
+      }
+    } else {
+      // ------------------------------------------------ rank 0: query terms + softmax
+      const int r = threadIdx.x - 128;           // TMEM lane == head row
+      const int wq = warp & 3;
+      const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+      const uint32_t precv_peer = map_to_peer(smem + L::kPrOff, 1);
+      const uint32_t pfull_peer = map_to_peer(&bar[F_P_FULL], 1);
+      TileIter<TILE> it;
+      it.start(pp, rng);
+      int g = 0;
+      int cq = 0;   // ring position in stages: kQStages per new query, one per tile
+      float m = -INFINITY, l = 0.f;
+      float fs = 0.f;   // this row's score factor: scale * log2(e) * kv_scale * sq
+      bool ok = true;
+      while (ok && it.valid) {
+        const UnitInfo ui = it.ui;
+        if (it.first()) {
+          if (it.newq) {
+            // (the softmax warps meet at named barriers, so every exit
+            // decision is made together through named_bar_and)
+            const bool qe = it.nq < 1 || wait_lazy(&bar[F_Q_EMPTY], (it.nq - 1) & 1);
+            const bool q0 = qe && wait_lazy(&bar[F_KFULL + cq % L::kNK], (cq / L::kNK) & 1);
+            const bool q1 =
+                q0 && wait_lazy(&bar[F_KFULL + (cq + 1) % L::kNK], ((cq + 1) / L::kNK) & 1);
+            if (!named_bar_and(1, 128, q1)) { ok = false; break; }
+            tc_fence_after();
+            // row r of 16-bit chunk c (8 latent, then RoPE) in the ring:
+            // 16-byte unit j at (j ^ (r & 7))
+            auto qrow_ptr = [&](int c) -> const uint8_t* {
+              const int qs = c / 5, k = c % 5;
+              return sK + ((cq + qs) % L::kNK) * L::kKStage + k * L::kChunk + r * 128;
+            };
+            const bool live = r < pp.H;   // rows past H hold the next query's rows
+            float amax = 0.f;
+            for (int c = 0; c < 9; ++c) {
+              const uint8_t* rowp = qrow_ptr(c);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                amax = amax8<BF16>(*reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4)),
+                                   amax);
+            }
+            if (!live) amax = 0.f;
+            // row scale sq = 2^(E - 8) with amax = f * 2^E, f in [0.5, 1):
+            // the row's largest value maps into [128, 256)
+            int E = 0;
+            frexpf(amax, &E);
+            const float inv_sq = live && amax > 0.f ? ldexpf(1.f, 8 - E) : 0.f;
+            fs = pp.scale_log2 * (amax > 0.f ? ldexpf(1.f, E - 8) : 1.f);
+            for (int c = 0; c < 8; ++c) {
+              const uint8_t* rowp = qrow_ptr(c);
+              uint32_t hi[16], lo[16];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                uint32_t h2[2], l2[2];
+                quantize8<BF16>(*reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4)),
+                                inv_sq, h2, l2);
+                hi[2 * j] = h2[0];
+                hi[2 * j + 1] = h2[1];
+                lo[2 * j] = l2[0];
+                lo[2 * j + 1] = l2[1];
+              }
+              // 64 values = 16 columns of 4 bytes
+              tmem_st16(tmem + lane_base + kQhiCol + c * 16, hi);
+              tmem_st16(tmem + lane_base + kQloCol + c * 16, lo);
+            }
+            {
+              // RoPE row: hi bytes -> units 0..3, lo bytes -> units 4..7 of
+              // row r of the 128-byte-swizzled sQr tile
+              const uint8_t* rowp = qrow_ptr(8);
+              uint32_t hi[16], lo[16];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                uint32_t h2[2], l2[2];
+                quantize8<BF16>(*reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4)),
+                                inv_sq, h2, l2);
+                hi[2 * j] = h2[0];
+                hi[2 * j + 1] = h2[1];
+                lo[2 * j] = l2[0];
+                lo[2 * j + 1] = l2[1];
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                *reinterpret_cast<uint4*>(sQr + sw128_offset(r, u)) =
+                    make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
+                *reinterpret_cast<uint4*>(sQr + sw128_offset(r, 4 + u)) =
+                    make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+              }
+            }
+            fence_proxy_async_smem();
+            tmem_wait_st();
+            tc_fence_before();
+            named_bar_sync(1, 128);   // every row has read the query's ring stages
+            if (threadIdx.x == 128) {
+              mbar_arrive(&bar[F_KEMPTY + cq % L::kNK]);
+              mbar_arrive(&bar[F_KEMPTY + (cq + 1) % L::kNK]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[F_QLAT_FULL]);
+            cq += L::kQStages;
+          }
+          m = -INFINITY;
+          l = 0.f;
+        }
+        const int sb = g & 1;
+        if (!named_bar_and(1, 128, wait_lazy(&bar[F_S_FULL + sb], (g >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float s[TILE];
+        // S in four 32-column loads, each folded into the row max before the
+        // next is issued
+        const int nvalid = min(TILE, ui.hi - (ui.lo + it.j * TILE));
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        {
+          const uint32_t sa = tmem + lane_base + kSCol + sb * TILE;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld32(sa + 32 * c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+              const int tt = 32 * c + t;
+              s[tt] = tt < nvalid ? __uint_as_float(v[t]) * fs : -INFINITY;
+              mx[t & 3] = fmaxf(mx[t & 3], s[tt]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[F_S_EMPTY + sb]);
+
+        // ---- online softmax in the log2 domain
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        bool need_rescale = false;
+        float alpha = 1.f;
+        if (it.first()) {
+          m = mt;
+        } else if (mt > m + kRescaleThresh) {
+          need_rescale = true;
+          alpha = fast_exp2(m - mt);
+          m = mt;
+        }
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int t = 0; t < TILE; ++t) {
+          s[t] = fast_exp2(s[t] - m);     // masked: exp2(-inf) = 0
+          ps[t & 3] += s[t];
+        }
+        l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+
+        // ---- P message for rank 1 (fp16 P; single outgoing buffer, free once
+        // rank 1 reports the previous message landed on F_MSG_FREE)
+        uint8_t* msg = sPs;
+        bool mfree = true;
+        if (threadIdx.x == 128 && g >= 1) mfree = wait_cl(&bar[F_MSG_FREE], (g - 1) & 1);
+        if (!named_bar_and(1, 128, mfree)) { ok = false; break; }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int uu = 0; uu < 8; ++uu) {
+            const int t = half * 64 + uu * 8;
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = pack2<false>(s[t + 2 * e], s[t + 2 * e + 1]);
+            *reinterpret_cast<uint4*>(msg + half * 16384 + sw128_offset(r, uu)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        reinterpret_cast<float*>(msg + L::kMsgAlpha)[r] = alpha;
+        reinterpret_cast<float*>(msg + L::kMsgL)[r] = l;
+        reinterpret_cast<float*>(msg + L::kMsgM)[r] = m;
+        const uint32_t any = __any_sync(0xffffffffu, need_rescale) ? 1u : 0u;
+        if (lane == 0) warp_flags[wq] = any;
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 128) {
+          const uint32_t flags = (warp_flags[0] | warp_flags[1] | warp_flags[2] | warp_flags[3]) |
+                                 (it.last() ? 2u : 0u);
+          *reinterpret_cast<volatile uint32_t*>(msg + L::kMsgHdr) = flags;
+          fence_proxy_async_smem();
+          if (g >= 2 && !wait_cl(&bar[F_PFREE + sb], ((g >> 1) - 1) & 1)) ok = false;
+          if (ok) {
+            bulk_copy_to_peer(precv_peer + sb * L::kMsgStride, msg, L::kMsgBytes,
+                              pfull_peer + sb * 8);
+            *msg_count = g + 1;
+          }
+        }
+        ok = named_bar_and(1, 128, ok && !*abort_flag);
+        it.advance(pp);
+        ++g;
+        cq += 1;
+      }
+    }
+  } else {
+    uint8_t* sV8 = smem + L::kV8Off;
+    uint8_t* sV16 = smem + L::kV16Off;
+    uint8_t* sPr = smem + L::kPrOff;
+    if (warp == 0) {
+      // ------------------------------------------------ rank 1: TMA producer (E4M3 V)
+      // Converged warp: lane (bb * 4 + c) issues 128-byte latent chunk c of
+      // box bb of each 64-token stage; lanes 0..nbox-1 hold the tile's box rows.
+      TileIter<TILE> it;
+      it.start(pp, rng);
+      int vs = 0;
+      bool ok = true;
+      const int nbox = TILE / br_v;            // boxes per tile (2, 4 or 8)
+      const int sub_boxes = L::kV8Sub / br_v;  // boxes per 64-token stage (1, 2 or 4)
+      const int vc = lane & 3, vb = lane >> 2;
+      const bool vlane = vb < sub_boxes;
+      const bool boxlane = lane < nbox;
+      int id_cur = boxlane ? fetch_id<TILE>(pp, it, br_v, lane, bs_shift) : 0;
+      while (it.valid) {
+        const UnitInfo ui = it.ui;
+        TileIter<TILE> nx = it;
+        nx.advance(pp);
+        const int id_next = boxlane ? fetch_id<TILE>(pp, nx, br_v, lane, bs_shift) : 0;
+        const int my_row = boxlane ? box_row<TILE>(pp, it, br_v, lane, id_cur, bs_shift) : 0;
+        const CUtensorMap* map = ui.current ? &tm_cur_v : &tm_kv_v;
+        uint8_t* dst = sV8 + vc * L::kV8Chunk + vb * br_v * 128;
+        for (int sub = 0; sub < TILE / L::kV8Sub; ++sub) {
+          const int st = vs % L::kNV8;
+          const int row = __shfl_sync(0xffffffffu, my_row, (sub * sub_boxes + vb) & 7);
+          if (vs >= L::kNV8 && !wait(&bar[F_V8EMPTY + st], ((vs / L::kNV8) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&bar[F_V8FULL + st], L::kV8Stage);
+          if (vlane) tma_load_2d(dst + st * L::kV8Stage, map, &bar[F_V8FULL + st], vc * 128, row);
+          ++vs;
+        }
+        if (!ok) break;
+        id_cur = id_next;
+        it = nx;
+      }
+      if (lane == 0)
+        for (int s = 0; s < L::kNV8 && s < vs; ++s) {
+          const int last = vs - 1 - ((vs - 1 - s) % L::kNV8);
+          mbar_wait(&bar[F_V8FULL + s], (last / L::kNV8) & 1, err);
+        }
+    } else if (warp == 1) {
+      // ------------------------------------------------ rank 1: MMA issuer (PV)
+      if (lane == 0) {
+        constexpr uint32_t idesc = make_idesc_f16(128, 256, false, false, true);   // fp16, V MN-major
+        const uint32_t v_base = smem_u32(sV16);
+        const uint32_t p_base = smem_u32(sPr);
+        TileIter<TILE> it;
+        it.start(pp, rng);
+        int g = 0, vs = 0, nfix = 0;
+        bool ok = true;
+        while (ok && it.valid) {
+          const int sb = g & 1;
+          if (!wait(&bar[F_P_FULL + sb], (g >> 1) & 1)) break;
+          const uint32_t hdr =
+              *reinterpret_cast<volatile uint32_t*>(sPr + sb * L::kMsgStride + L::kMsgHdr);
+          const bool first = it.first();
+          if (first && it.k >= 1 && !wait(&bar[F_O_EMPTY], (it.k - 1) & 1)) break;
+          if (hdr & 1u) {
+            if (!wait(&bar[F_O_FIXED], nfix & 1)) break;
+            ++nfix;
+          }
+          const uint32_t pa = p_base + sb * L::kMsgStride;
+          for (int sub = 0; sub < TILE / L::kV16Sub; ++sub) {
+            const int st = vs % L::kNV16;
+            if (!wait(&bar[F_V16FULL + st], (vs / L::kNV16) & 1)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t vb = v_base + st * L::kV16Stage;
+#pragma unroll
+            for (int kk = 0; kk < L::kV16Sub / 16; ++kk) {
+              const int tok = sub * L::kV16Sub + kk * 16;
+              const uint64_t ad = make_desc_sw128(pa + (tok >> 6) * 16384 + (tok & 63) * 2, 16, 1024);
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const uint64_t bd =
+                    make_desc_sw128(vb + half * 4 * L::kV16Chunk + kk * 2048, L::kV16Chunk, 1024);
+                umma_ss(tmem + half * 256, ad, bd, idesc, (first && sub == 0 && kk == 0) ? 0u : 1u);
+              }
+            }
+            umma_commit(&bar[F_V16EMPTY + st]);
+            ++vs;
+          }
+          if (!ok) break;
+          umma_commit(&bar[F_PV_DONE + sb]);
+          it.advance(pp);
+          ++g;
+        }
+        umma_commit(&bar[F_MMA_DONE_B]);
+        mbar_wait(&bar[F_MMA_DONE_B], 0, err);
+      }
+    } else if (warp == 2) {
+      // ------------------------------------------------ rank 1: hand P buffers back
+      if (lane == 0) {
+        const uint32_t pfree_peer = map_to_peer(&bar[F_PFREE], 0);
+        TileIter<TILE> it;
+        it.start(pp, rng);
+        int g = 0;
+        while (it.valid) {
+          const int sb = g & 1;
+          if (!wait(&bar[F_PV_DONE + sb], (g >> 1) & 1)) break;
+          if (!wait(&bar[F_META_READ + sb], (g >> 1) & 1)) break;
+          mbar_arrive_expect_tx(&bar[F_P_FULL + sb], L::kMsgBytes);   // tile g + 2
+          mbar_arrive_remote(pfree_peer + sb * 8);
+          it.advance(pp);
+          ++g;
+        }
+      }
+    } else if (warp == 3) {
+      // ------------------------------------------------ rank 1: zeros of empty parts
+      for (int u = cid; u < pp.num_units; u += ncl) {
+        const UnitInfo ui = unit_info<TILE>(pp, u);
+        if (ui.ntiles != 0) continue;
+        const int64_t tok = static_cast<int64_t>(ui.b) * pp.q_len + ui.i;
+        for (int h = 0; h < pp.H; ++h) {
+          const int64_t e0 = part_row(pp, tok, ui.p, h) * 512;
+          if (pp.part_dtype == kFP32) {
+            float4* o = reinterpret_cast<float4*>(static_cast<float*>(pp.o_part) + e0);
+            for (int c = lane; c < 128; c += 32) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+          } else {
+            uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(pp.o_part) + e0);
+            for (int c = lane; c < 64; c += 32) o[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      // ------------------------------------------------ rank 1: P landing watcher
+      // Reports each P message to rank 0 once it has landed (the sender's
+      // single buffer is then free) and counts them for the final drain.
+      if (lane == 0) {
+        const uint32_t msgfree_peer = map_to_peer(&bar[F_MSG_FREE], 0);
+        TileIter<TILE> it;
+        it.start(pp, rng);
+        int g = 0;
+        while (it.valid) {
+          if (!wait(&bar[F_P_FULL + (g & 1)], (g >> 1) & 1)) break;
+          *msg_count = g + 1;
+          mbar_arrive_remote(msgfree_peer);
+          it.advance(pp);
+          ++g;
+        }
+      }
+    } else {
+      // ------------------------------------------------ rank 1: V widening, O rescale, epilogue
+      const int r = threadIdx.x - 128;
+      const int wq = warp & 3;
+      const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+      // V widening: warp wq takes tokens [8 wq, 8 wq + 8) of each 32-token
+      // fp16 stage, lane = (token t_in, 16-byte unit uu); per step one
+      // 64-latent group q: 8 tokens x 64 bytes read, 8 x 128 bytes written
+      // (both 128-byte-swizzled, so every access hits each bank 4 times).
+      // Tokens past the tile's valid ones (slots after the history's end in
+      // its last page, whatever bytes they hold) are written as zeros: their
+      // P is 0, and 0 times a NaN code would still be NaN.
+      const int t_in = lane >> 2, uu = lane & 3;
+      const int tv = 8 * wq + t_in;   // token within the fp16 stage
+      int v16 = 0;
+      auto widen = [&](bool live) -> bool {
+        const int s8 = v16 >> 1, h = v16 & 1;
+        const int st8 = s8 % L::kNV8, st16 = v16 % L::kNV16;
+        if (h == 0 && !wait_lazy(&bar[F_V8FULL + st8], (s8 / L::kNV8) & 1)) return false;
+        if (v16 >= L::kNV16 && !wait_lazy(&bar[F_V16EMPTY + st16], ((v16 / L::kNV16) - 1) & 1))
+          return false;
+        const uint8_t* src = sV8 + st8 * L::kV8Stage;
+        uint8_t* dst = sV16 + st16 * L::kV16Stage;
+        const int row8 = h * L::kV16Sub + tv;   // row within the E4M3 stage
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          // latent bytes [64 q + 16 uu, +16) of the token
+          uint4 x = *reinterpret_cast<const uint4*>(
+              src + (q >> 1) * L::kV8Chunk + sw128_offset(row8, (q & 1) * 4 + uu));
+          if (!live) x = make_uint4(0, 0, 0, 0);
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+          uint32_t f[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            f[2 * k] = e4m3x2_to_f16x2(w[k] & 0xFFFFu);
+            f[2 * k + 1] = e4m3x2_to_f16x2(w[k] >> 16);
+          }
+          uint8_t* o = dst + q * L::kV16Chunk;
+          *reinterpret_cast<uint4*>(o + sw128_offset(tv, 2 * uu)) = make_uint4(f[0], f[1], f[2], f[3]);
+          *reinterpret_cast<uint4*>(o + sw128_offset(tv, 2 * uu + 1)) =
+              make_uint4(f[4], f[5], f[6], f[7]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bar[F_V16FULL + st16]);
+          if (h == 1) mbar_arrive(&bar[F_V8EMPTY + st8]);
+        }
+        ++v16;
+        return true;
+      };
+      // Epilogue of a piece: O * (kv_scale / l) and its LSE, after the
+      // piece's last PV MMAs.  It runs once the next tile's first two fp16 V
+      // stages are written (those need only the previous tile's MMAs), so
+      // the V widening never waits on it.
+      struct Pending {
+        int64_t row_out;
+        int slot;
+        float lse2, mul;
+        int g;
+        bool whole, on;
+      } pend;
+      pend.on = false;
+      auto epilogue = [&]() -> bool {
+        if (!wait_lazy(&bar[F_PV_DONE + (pend.g & 1)], (pend.g >> 1) & 1)) return false;
+        tc_fence_after();
+        if (pend.whole) {
+          for (int c0 = 0; c0 < 512; c0 += 64) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tmem + lane_base + c0, v0);
+            tmem_ld32(tmem + lane_base + c0 + 32, v1);
+            tmem_wait_ld();
+            if (r < pp.H) {
+              store_row32(pp.o_part, pend.row_out * 512 + c0, v0, pend.mul, pp.part_dtype);
+              store_row32(pp.o_part, pend.row_out * 512 + c0 + 32, v1, pend.mul, pp.part_dtype);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar[F_O_EMPTY]);
+          if (r < pp.H) pp.lse_part[pend.row_out] = pend.lse2 * kLn2;
+        } else {
+          // a piece of a unit split across pairs: O / l and the LSE (log2)
+          // parked in this pair's workspace slot for the merge kernel
+          for (int c0 = 0; c0 < 512; c0 += 64) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tmem + lane_base + c0, v0);
+            tmem_ld32(tmem + lane_base + c0 + 32, v1);
+            tmem_wait_ld();
+            const int64_t e = (static_cast<int64_t>(pend.slot) * 128 + r) * 512 + c0;
+            store_row32(pp.ws_o, e, v0, pend.mul, pp.part_dtype);
+            store_row32(pp.ws_o, e + 32, v1, pend.mul, pp.part_dtype);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar[F_O_EMPTY]);
+          pp.ws_lse[pend.slot * 128 + r] = pend.lse2;
+        }
+        pend.on = false;
+        return true;
+      };
+      TileIter<TILE> it;
+      it.start(pp, rng);
+      int g = 0;
+      bool ok = true;
+      while (ok && it.valid) {
+        const UnitInfo ui = it.ui;
+        const int sb = g & 1;
+        const int nvalid = min(TILE, ui.hi - (ui.lo + it.j * TILE));
+        // (1) the tile's first two fp16 V stages (they need only the
+        // previous tile's MMAs to be done with their buffers)
+        if (!widen(tv < nvalid) || !widen(L::kV16Sub + tv < nvalid)) { ok = false; break; }
+        // (2) the epilogue of the piece that ended with the previous tile
+        if (pend.on && !epilogue()) { ok = false; break; }
+        // (3) this tile's message header
+        if (!wait_lazy(&bar[F_P_FULL + sb], (g >> 1) & 1)) { ok = false; break; }
+        const uint8_t* msg = sPr + sb * L::kMsgStride;
+        const uint32_t hdr = *reinterpret_cast<const volatile uint32_t*>(msg + L::kMsgHdr);
+        const float alpha = reinterpret_cast<const float*>(msg + L::kMsgAlpha)[r];
+        const float lsum = reinterpret_cast<const float*>(msg + L::kMsgL)[r];
+        const float m2 = reinterpret_cast<const float*>(msg + L::kMsgM)[r];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[F_META_READ + sb]);
+        // (4) O *= alpha before PV of this tile (never on a piece's first tile)
+        if (hdr & 1u) {
+          if (!wait_lazy(&bar[F_PV_DONE + ((g - 1) & 1)], ((g - 1) >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          for (int c0 = 0; c0 < 512; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + c0, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
+            tmem_st32(tmem + lane_base + c0, v);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar[F_O_FIXED]);
+        }
+        // (5) the tile's other two fp16 V stages
+        if (!widen(2 * L::kV16Sub + tv < nvalid) || !widen(3 * L::kV16Sub + tv < nvalid)) {
+          ok = false;
+          break;
+        }
+        // (6) a piece ends with this tile: its epilogue follows the next
+        // tile's first V stages (or the loop)
+        if (hdr & 2u) {
+          pend.on = true;
+          pend.g = g;
+          pend.lse2 = m2 + __log2f(lsum);
+          pend.mul = pp.out_scale / lsum;
+          pend.whole = it.whole();
+          pend.slot = 2 * cid + (it.u == rng.u_begin ? 0 : 1);
+          pend.row_out = part_row(pp, static_cast<int64_t>(ui.b) * pp.q_len + ui.i, ui.p, r);
+        }
+        it.advance(pp);
+        ++g;
+      }
+      if (ok && pend.on) epilogue();
+    }
+  }
+
+  // every tensor-memory access of this thread has completed before TMEM is freed
+  __syncwarp();
+  tmem_wait_st();
+  tmem_wait_ld();
+  tc_fence_before();
+  __syncthreads();
+  if (pp.split && rank == 1 && threadIdx.x == 0) record_split_unit<TILE>(pp, cid, rng, shares, split);
+  cluster_sync();
+  if (rank == 1 && threadIdx.x == 64) {
+    // Drain the P messages rank 0 sent that the watcher never saw land (it
+    // stops early when a wait runs out): rank 0 must not exit while its
+    // copies still read its buffer, nor rank 1 while they still write here.
+    const uint32_t sent_addr = map_to_peer(const_cast<int*>(msg_count), 0);
+    int sent;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(sent) : "r"(sent_addr) : "memory");
+    for (int k = *msg_count; k < sent; ++k) mbar_wait(&bar[F_P_FULL + (k & 1)], (k >> 1) & 1, err);
+  }
+  cluster_sync();   // no DSMEM traffic into either CTA after this point
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- launcher
+// Shared-memory limit and co-resident pairs of the kernel on the current
+// device (cached per device ordinal under a lock, as for the 16-bit kernel).
+template <bool BF16>
+static int prepare_partial_fp8(int* clusters) {
+  static int cache[64] = {0};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    auto kern = mla_partial_fp8_kernel<BF16>;
+    constexpr int smem = Fp8Smem::kTotal;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int mc = 0;
+    if (cudaOccupancyMaxActiveClusters(&mc, kern, &cfg) != cudaSuccess || mc < 1) return -1;
+    cache[dev] = std::min(mc, 256);
+  }
+  *clusters = cache[dev];
+  return 0;
+}
+
+int partial_fp8_max_clusters() {
+  int a = 0, b = 0;
+  if (prepare_partial_fp8<true>(&a) != 0 || prepare_partial_fp8<false>(&b) != 0) return -1;
+  return std::min(a, b);
+}
+
+template <bool BF16>
+static int launch_partial_fp8_t(const CUtensorMap& qlat, const CUtensorMap& qpe,
+                                const CUtensorMap& kv, const CUtensorMap& cur,
+                                const CUtensorMap& kv_v, const CUtensorMap& cur_v,
+                                const PartialParams& pp, cudaStream_t stream) {
+  int max_clusters = 0;
+  if (prepare_partial_fp8<BF16>(&max_clusters) != 0) return -1;
+  const int clusters = pp.split ? pp.split : std::max(1, std::min(pp.num_units, max_clusters));
+  if (clusters > max_clusters) return -1;
+  mla_partial_fp8_kernel<BF16><<<dim3(2 * clusters), dim3(256), Fp8Smem::kTotal, stream>>>(
+      qlat, qpe, kv, cur, kv_v, cur_v, pp);
+  return pp.split ? launch_partial_merge(pp, clusters, stream) : 0;
+}
+
+int launch_partial_fp8(const CUtensorMap& qlat, const CUtensorMap& qpe, const CUtensorMap& kv,
+                       const CUtensorMap& cur, const CUtensorMap& kv_v, const CUtensorMap& cur_v,
+                       const PartialParams& pp, bool bf16, cudaStream_t stream) {
+  return bf16 ? launch_partial_fp8_t<true>(qlat, qpe, kv, cur, kv_v, cur_v, pp, stream)
+              : launch_partial_fp8_t<false>(qlat, qpe, kv, cur, kv_v, cur_v, pp, stream);
+}
+
+}  // namespace mla

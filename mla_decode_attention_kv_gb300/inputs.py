@@ -137,26 +137,24 @@ class DecodeProblem:
         return self.cfg.num_shards + (1 if self.kv_cur is not None else 0)
 
 
-def _e4m3_positive_values() -> np.ndarray:
-    """Values of the E4M3 codes 0x00..0x7E (sign 0, 4 exponent bits with bias
-    7, 3 mantissa bits; exponent field 0 is subnormal; 0x7F is NaN)."""
-    codes = np.arange(0x7F)
-    e, m = codes >> 3, codes & 7
-    return np.where(e == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * 2.0 ** (e - 7.0))
-
-
 def _round_e4m3(x: np.ndarray) -> np.ndarray:
-    """float -> E4M3 bytes: nearest representable value, ties to the even
-    code (mantissa LSB 0), magnitudes above 448 saturate to 448."""
-    vals = _e4m3_positive_values()
-    a = np.minimum(np.abs(np.asarray(x, dtype=np.float64)), vals[-1])
-    hi = np.clip(np.searchsorted(vals, a, side="left"), 0, len(vals) - 1)
-    lo = np.maximum(hi - 1, 0)
-    d_lo, d_hi = a - vals[lo], vals[hi] - a
-    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
-    code = np.where(a == vals[hi], hi, np.where(pick_hi, hi, lo)).astype(np.uint8)
-    sign = (np.signbit(np.asarray(x, dtype=np.float64)) & (code != 0)).astype(np.uint8)
-    return code | (sign << np.uint8(7))
+    """float32 -> E4M3 bytes (sign bit, 4 exponent bits with bias 7, 3 mantissa
+    bits, exponent field 0 subnormal): nearest value, ties to the even code,
+    magnitudes past 448 saturate to 448 (0x7E); -0 and values that round to
+    zero give 0x00.  Below 2^-6 the codes are the subnormal steps m * 2^-9,
+    m = rint(|x| * 2^9) (8 is the first normal code); above, the float32
+    mantissa is rounded to 3 bits on the integer bits (a carry moves into the
+    exponent) and the exponent rebased from 127 to 7."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32) & np.uint32(0x7FFFFFFF)
+    a = u.view(np.float32)
+    small = a < np.float32(2.0 ** -6)
+    sub = np.rint(np.where(small, a, 0) * np.float32(512.0)).astype(np.int32)
+    r = u + (np.uint32(0x7FFFF) + ((u >> np.uint32(20)) & np.uint32(1)))
+    norm = (r >> np.uint32(20)).view(np.int32) - np.int32(120 << 3)
+    code = np.where(small, sub, np.minimum(norm, 0x7E)).astype(np.uint8)
+    neg = (x.view(np.uint32) >> np.uint32(31)).astype(np.uint8) & (code != 0)
+    return code | (neg << np.uint8(7))
 
 
 def round_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:

@@ -194,11 +194,13 @@ def _all_heads(problem):
 
 # ---------------------------------------------------------------- partials
 def decode_partials(problem, batch: Optional[Sequence[int]] = None,
-                    heads: Optional[Sequence[int]] = None):
+                    heads: Optional[Sequence[int]] = None, queries=None):
     """Per-shard (and CURRENT) partial outputs and LSEs.
 
     Returns o_part [nb, q, P, nh, 512] and lse_part [nb, q, P, nh] for the
-    requested sequences and heads, P = num_shards (+1 for CURRENT, last)."""
+    requested sequences and heads, P = num_shards (+1 for CURRENT, last).
+    queries: optional (b, i, heads) -> (q_abs, q_pe) float64 rows used in
+    place of the problem's stored queries."""
     cfg = problem.cfg
     batch = list(range(cfg.batch)) if batch is None else list(batch)
     heads = _all_heads(problem) if heads is None else np.asarray(heads)
@@ -210,7 +212,7 @@ def decode_partials(problem, batch: Optional[Sequence[int]] = None,
         cur = _current(problem, b)
         bounds = shard_bounds(hist.shape[0], cfg.num_shards, cfg.block_size)
         for i in range(cfg.q_len):
-            qa, qp = _queries(problem, b, i, heads)
+            qa, qp = (queries or (lambda b_, i_, h_: _queries(problem, b_, i_, h_)))(b, i, heads)
             for s, (lo, hi) in enumerate(bounds):
                 o_part[bi, i, s], lse_part[bi, i, s] = segment_attention(
                     qa, qp, hist[lo:hi], cfg.scale)

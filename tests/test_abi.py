@@ -73,6 +73,36 @@ def test_partial_host_checks(lib):
     assert _partial(lib, ws=ctypes.c_void_p(0x10010), wsb=1 << 20) == 4   # workspace not 256-aligned
 
 
+def _partial_fp8(lib, kv_scale=0.01, **over):
+    args = dict(q_abs=FAKE, q_pe=FAKE, kv=FAKE, table=FAKE, lens=FAKE, cur=None, B=2, q=1,
+                H=128, nb=10, bs=32, mb=5, S=2, scale=0.07, idt=0, pdt=0, o=FAKE, l=FAKE,
+                err=None, ws=None, wsb=0, slices=1)
+    args.update(over)
+    a = args
+    return lib.mla_dcp_decode_partial_fp8(a["q_abs"], a["q_pe"], a["kv"], a["table"], a["lens"],
+                                          a["cur"], a["B"], a["q"], a["H"], a["nb"], a["bs"],
+                                          a["mb"], a["S"], a["scale"], kv_scale, a["idt"],
+                                          a["pdt"], a["o"], a["l"], a["err"], a["ws"], a["wsb"],
+                                          a["slices"], None)
+
+
+def test_partial_fp8_host_checks(lib):
+    """The E4M3-cache entry point runs the same checks, plus kv_scale."""
+    assert _partial_fp8(lib, q_abs=None) == 1
+    assert _partial_fp8(lib, idt=2) == 3
+    assert _partial_fp8(lib, H=129) == 2
+    assert _partial_fp8(lib, q=65) == 2
+    assert _partial_fp8(lib, S=65) == 5
+    assert _partial_fp8(lib, bs=48) == 6
+    assert _partial_fp8(lib, kv=ODD) == 4
+    assert _partial_fp8(lib, kv_scale=0.0) == 2
+    assert _partial_fp8(lib, kv_scale=-1.0) == 2
+    assert _partial_fp8(lib, kv_scale=float("inf")) == 2
+    assert _partial_fp8(lib, kv_scale=float("nan")) == 2
+    assert _partial_fp8(lib, kv_scale=1e38, scale=1e3) == 2     # scale * kv_scale overflows
+    assert _partial_fp8(lib, slices=3) == 2                     # 3 does not divide 128
+
+
 def test_workspace_size_rejects_bad_sizes(lib):
     assert lib.mla_dcp_decode_partial_workspace_size(0, 1, 2, 0) == 0
     assert lib.mla_dcp_decode_partial_workspace_size(2, 65, 2, 0) == 0
