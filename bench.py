@@ -61,6 +61,8 @@ WORKLOAD_TEXT = {
               "16 shards, block 32, random block table, fp16 cache",
     "verylong": "very long context: batch 16, 128 heads, 131072 KV tokens, 16 shards, bf16, "
                 "fused combine + V-up",
+    "verylong_fp8": "very long context over an FP8 (E4M3) latent cache, kv_scale 2^-8: batch 16, "
+                    "128 heads, 131072 KV tokens, 16 shards, bf16 queries, fused combine + V-up",
     "tiny": "tiny: batch 1, 16 heads, 256 history tokens in 2 shards + 1 current token",
 }
 
@@ -111,13 +113,15 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_sha() -> str:
-    """Hash of the partial kernel's sources with comments and blank lines
-    removed, so that editing a comment does not disown the ncu counters."""
+def kernel_source_sha(fp8: bool = False) -> str:
+    """Hash of the partial kernel's sources (the 16-bit or the E4M3-cache
+    kernel) with comments and blank lines removed, so that editing a comment
+    does not disown the ncu counters."""
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_decode_attention_kv_gb300", "csrc")
-    for name in ("partial.cu", "ptx.cuh", "common.cuh", "kernels.cuh"):
+    main = "partial_fp8.cu" if fp8 else "partial.cu"
+    for name in (main, "partial_sched.cuh", "ptx.cuh", "common.cuh", "kernels.cuh"):
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
@@ -136,7 +140,7 @@ def profile_counters(config_name: str):
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("kernel_source_sha") != kernel_source_sha():
+    if d.get("kernel_source_sha") != kernel_source_sha(inputs.CONFIGS[config_name].kv_dtype == "e4m3"):
         return None
     return d
 
@@ -256,12 +260,18 @@ class DeviceWorkload:
         def t16(a):
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(self.dt)
 
+        def t8(a):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).to(dev)
+
+        self.fp8 = cfg.cache_dtype == "e4m3"
+        self.kv_scale = cfg.kv_scale if self.fp8 else None
+        tk = t8 if self.fp8 else t16
         self.q_abs, self.q_pe, W0 = t16(prob.q_abs), t16(prob.q_pe), t16(prob.W_UV)
-        cache0 = t16(prob.kv_cache)
-        self.kv_cur = t16(prob.kv_cur) if prob.kv_cur is not None else None
+        cache0 = tk(prob.kv_cache)
+        self.kv_cur = tk(prob.kv_cur) if prob.kv_cur is not None else None
         self.table = torch.from_numpy(prob.block_table).to(dev)
         self.lens = torch.from_numpy(prob.seq_lens).to(dev)
-        self.per_layer = cache0.numel() * 2 + W0.numel() * 2
+        self.per_layer = cache0.numel() * cache0.element_size() + W0.numel() * 2
         self.layers = layers or max(2, math.ceil(4 * L2_BYTES / self.per_layer))
         self.caches = [cache0] + [cache0.clone() for _ in range(self.layers - 1)]
         self.Ws = [W0] + [W0.clone() for _ in range(self.layers - 1)]
@@ -278,7 +288,7 @@ class DeviceWorkload:
         self.api.mla_dcp_decode_partial(
             self.q_abs, self.q_pe, self.caches[li], self.table, self.lens, self.cfg.num_shards,
             kv_cur=self.kv_cur, scale=self.cfg.scale, o_part=self.o_part,
-            lse_part=self.lse_part, err_flag=self.err, stream=stream)
+            lse_part=self.lse_part, err_flag=self.err, stream=stream, kv_scale=self.kv_scale)
         if ev is not None:
             ev[1].record(stream)
         self.api.mla_lse_combine_vup(self.o_part, self.lse_part, self.Ws[li], out=self.out,
@@ -318,7 +328,7 @@ class DeviceWorkload:
         parts = [("q_abs", prob.q_abs.view(np.int16)), ("q_pe", prob.q_pe.view(np.int16)),
                  ("table", prob.block_table), ("lens", prob.seq_lens)]
         if prob.kv_cur is not None:
-            parts.append(("kv_cur", prob.kv_cur.view(np.int16)))
+            parts.append(("kv_cur", prob.kv_cur))
         offs, off = {}, 0
         for name, a in parts:
             offs[name] = off
@@ -359,7 +369,8 @@ class DeviceWorkload:
             self.api.decode_step(v["q_abs"], v["q_pe"], self.caches[li], v["table"], v["lens"],
                                  self.Ws[li], cfg.num_shards, kv_cur=v.get("kv_cur"),
                                  scale=cfg.scale, o_part=self.o_part, lse_part=self.lse_part,
-                                 out=d_out[k], err_flag=self.err, stream=stream)
+                                 out=d_out[k], err_flag=self.err, stream=stream,
+                                 kv_scale=self.kv_scale)
             ev_used[k].record(stream)
             with torch.cuda.stream(copy):
                 copy.wait_event(ev_used[k])
@@ -399,7 +410,8 @@ class DeviceWorkload:
             roof = {"bound": "tensor", "achieved": round(tc_ach, 1), "peak": peaks["bf16_tflops"],
                     "unit": "TFLOP/s", "frac": round(tc_frac, 4)}
         roof["traffic"] = traffic_from_profile(self.name)
-        roof["kernel"] = "mla_partial_kernel (+ mla_partial_merge_kernel)"
+        roof["kernel"] = ("mla_partial_fp8_kernel" if self.fp8 else "mla_partial_kernel") + \
+            " (+ mla_partial_merge_kernel)"
         roof["kernel_ms"] = round(partial_ms, 5)
         roof["alg_bytes_per_launch"] = wm["partial_bytes"]
         roof["alg_flops_per_launch"] = wm["partial_flops"]
@@ -617,7 +629,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=sorted(inputs.CONFIGS), default="verylong")
-    ap.add_argument("--extra", default="dsv3,mtp,ragged",
+    ap.add_argument("--extra", default="dsv3,mtp,ragged,verylong_fp8",
                     help="other workloads timed device-only (comma list, or none)")
     ap.add_argument("--layers", type=int, default=0, help="layer caches rotated (0 = auto)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,

@@ -184,16 +184,18 @@ int mla_dcp_decode_partial_sliced(const void* q_abs, const void* q_pe, const voi
  * mla_dcp_decode_partial on those values.
  *
  * Differences from mla_dcp_decode_partial_sliced:
- *   kv_cache   [num_blocks, block_size, 576] bytes (E4M3); slots of a last
- *              block past L_b may hold any bytes
+ *   kv_cache   [num_blocks, block_size, 576] bytes (E4M3); as for the 16-bit
+ *              cache, the slots of a last block past L_b are read with the
+ *              block and weighted by 0, so they must not hold the NaN codes
  *   kv_cur     [B, q_len, 576] bytes (E4M3, the same kv_scale), or NULL
  *   kv_scale   > 0 and finite (scale * kv_scale too); MLA_ERR_BAD_SHAPE otherwise
  * Precision: the tensor cores multiply the cache bytes by the query in two
  * E4M3 terms (a power-of-two row scale, then the rounded row and its rounded
  * remainder), which keeps |error of q| <= 2^-8 |q| + 2^-17 max|q row|,
- * about the precision of bf16; P is rounded to fp16.  The cache must not
- * hold the NaN codes in visible slots.  Every other argument, result and
- * error (including the workspace, of the same size) as
+ * about the precision of bf16; the softmax weights p (at most 4 times the
+ * running maximum) go to the PV product in the same two-term form of 2^6 p
+ * (rounded to fp16 first): |error of p| <= 2^-7 p + 2^-16.  Every other argument, result and error
+ * (including the workspace, of the same size) as
  * mla_dcp_decode_partial_sliced.
  */
 int mla_dcp_decode_partial_fp8(const void* q_abs, const void* q_pe, const void* kv_cache,

@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(256, 1)
       const int c0 = (warp >> 2) * 32;   // warps 0-3: rows 0-31, warps 4-7: rows 32-63
       uint32_t r[32];
       tmem_ld32(tmem + (static_cast<uint32_t>(wq * 32) << 16) + c0, r);
-      tmem_wait_ld();
+      tmem_wait_ld(r);
       uint16_t* o = static_cast<uint16_t*>(out);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -651,7 +651,7 @@ __global__ void __launch_bounds__(256, 1)
       for (int n0 = 0; n0 < nvalid; n0 += 32) {
         uint32_t r[32];
         tmem_ld32(tmem + lane_base + n0, r);
-        tmem_wait_ld();
+        tmem_wait_ld(r);
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           if (n0 + i < nvalid) {

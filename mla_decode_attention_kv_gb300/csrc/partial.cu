@@ -213,7 +213,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   TileRange rng;
   Shares shares;
   bool split = false;
-  partition_tiles<TILE>(pp, cid, ncl, rng, shares, split);
+  partition_tiles<TILE, 256>(pp, cid, ncl, rng, shares, split);
 
   const Waits waits{pp.spin_limit, abort_flag, err};
   auto wait = [&](uint64_t* b, uint32_t parity) { return waits.wait(b, parity); };
@@ -457,7 +457,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           for (int c = 0; c < 4; ++c) {
             uint32_t v[32];
             tmem_ld32(sa + 32 * c, v);
-            tmem_wait_ld();
+            tmem_wait_ld(v);
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
               const int tt = 32 * c + t;
@@ -712,7 +712,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           for (int c0 = 0; c0 < 512; c0 += 32) {
             uint32_t v[32];
             tmem_ld32(tmem + lane_base + c0, v);
-            tmem_wait_ld();
+            tmem_wait_ld(v);
 #pragma unroll
             for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
             tmem_st32(tmem + lane_base + c0, v);
@@ -736,7 +736,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
               uint32_t v0[32], v1[32];
               tmem_ld32(tmem + lane_base + c0, v0);
               tmem_ld32(tmem + lane_base + c0 + 32, v1);
-              tmem_wait_ld();
+              tmem_wait_ld(v0, v1);
               if (r < pp.H) {
                 store_row32(pp.o_part, row_out * 512 + c0, v0, inv_l, pp.part_dtype);
                 store_row32(pp.o_part, row_out * 512 + c0 + 32, v1, inv_l, pp.part_dtype);
@@ -755,7 +755,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
               uint32_t v0[32], v1[32];
               tmem_ld32(tmem + lane_base + c0, v0);
               tmem_ld32(tmem + lane_base + c0 + 32, v1);
-              tmem_wait_ld();
+              tmem_wait_ld(v0, v1);
               const int64_t e = (static_cast<int64_t>(slot) * 128 + r) * 512 + c0;
               store_row32(pp.ws_o, e, v0, inv_l, pp.part_dtype);
               store_row32(pp.ws_o, e + 32, v1, inv_l, pp.part_dtype);

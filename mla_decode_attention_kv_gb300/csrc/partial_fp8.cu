@@ -16,17 +16,28 @@
 //     |e| <= 2^-8 |q| + 2^-17 max|q_row|, about the precision of bf16.  S is
 //     accumulated as Q_hi K^T + Q_lo K^T (two MMAs per k-step: the tensor
 //     work of the 16-bit kernel, on half the bytes).
-//   rank 1 (PV CTA): V stages of E4M3 bytes are widened to fp16 in shared
-//     memory by the four epilogue warps (exact: every E4M3 value is an fp16
-//     value), then O += P V as kind::f16 MMAs with P in fp16.
-// kv_scale is folded into the softmax scale and into the epilogue's 1 / l.
+//   rank 1 (PV CTA): O += P V as kind::f8f6f4 MMAs straight on the E4M3 V
+//     bytes that TMA lands (V as the MN-major B operand: latent-contiguous
+//     token rows, as the cache stores them), with P in the same two-term
+//     form: p' = 2^6 p (p <= 2^2 under the lazy-rescale threshold, so
+//     p' <= 256 and the bulk of p' lies in E4M3's normal range),
+//     hi = rn(p'), lo = rn(p' - hi).  Rank 0 sends p' in fp16 (its exp2 and
+//     the fp16 packing are the softmax's whole conversion work); rank 1's
+//     epilogue warps split it into the two E4M3 terms in place, so the
+//     conversion work of a tile is shared by the two SMs.
+// kv_scale is folded into the softmax scale and into the epilogue's 1 / l
+// (l is the row sum of p', so the 2^6 cancels).
 //
-// Warp roles (256 threads per CTA):
+// Warp roles (384 threads per CTA; two 4-warp groups per row set, group
+// A = w4-7, group B = w8-11, thread = TMEM lane = head row):
 //   rank 0: w0 TMA producer (query chunks, K tiles), w1 MMA issuer, w2-3 LSE
-//           of empty parts, w4-7 query quantisation + softmax (thread = row)
+//           of empty parts; group A quantises each new query, then both
+//           groups run the softmax of a tile, A on its columns 0..63 and B
+//           on 64..127 (the row max is exchanged through shared memory)
 //   rank 1: w0 TMA producer (E4M3 V), w1 MMA issuer, w2 hands P buffers
-//           back, w3 zeros of empty parts + P landing watcher, w4-7 V
-//           widening, O rescale and epilogue (thread = row)
+//           back, w3 zeros of empty parts + P landing watcher; groups A / B
+//           rescale O and write the epilogue of latent columns 0..255 /
+//           256..511
 // Every wait is bounded, as in the 16-bit kernel.
 #include <cuda_fp8.h>
 #include <mutex>
@@ -47,36 +58,33 @@ struct Fp8Smem {
   static constexpr int kV8Sub = 64;                  // tokens per E4M3 V stage
   static constexpr int kV8Chunk = kV8Sub * 128;      // 128 latent bytes x 64 tokens (8 KB)
   static constexpr int kV8Stage = 4 * kV8Chunk;      // 32 KB
-  static constexpr int kNV8 = 2;
-  static constexpr int kV16Sub = 32;                 // tokens per fp16 V stage
-  static constexpr int kV16Chunk = kV16Sub * 128;    // 64 latent x 32 tokens, fp16 (4 KB)
-  static constexpr int kV16Stage = 8 * kV16Chunk;    // 32 KB
-  static constexpr int kNV16 = 2;
-  // P message: P [128 rows x 128 tokens] fp16 as two 64-token SW128 chunks,
-  // alpha[128], lsum[128], m[128], header.
+  static constexpr int kNV8 = 4;
+  // P message: P' [128 rows x 128 tokens] fp16 as two 64-token 128-byte-
+  // swizzled 16 KB tiles (rewritten in place by rank 1 as [hi | lo] E4M3
+  // bytes of the same 64 tokens per 128-byte row), alpha[128], the row sums
+  // of the two column halves lA[128] and lB[128], m[128], header.
   static constexpr int kMsgP = 2 * 16384;
   static constexpr int kMsgAlpha = kMsgP;
-  static constexpr int kMsgL = kMsgAlpha + 512;
-  static constexpr int kMsgM = kMsgL + 512;
+  static constexpr int kMsgLA = kMsgAlpha + 512;
+  static constexpr int kMsgLB = kMsgLA + 512;
+  static constexpr int kMsgM = kMsgLB + 512;
   static constexpr int kMsgHdr = kMsgM + 512;
-  static constexpr int kMsgBytes = kMsgHdr + 16;     // 34320, multiple of 16
-  static constexpr int kMsgStride = 34816;           // 1024-aligned slot
+  static constexpr int kMsgBytes = kMsgHdr + 16;     // 34832, multiple of 16
+  static constexpr int kMsgStride = 35840;           // 1024-aligned slot
   // rank 0
   static constexpr int kKOff = 0;
   static constexpr int kQr8Off = kKOff + kNK * kKStage;   // 163840: query RoPE, hi | lo bytes
   static constexpr int kPsOff = kQr8Off + 16384;          // 180224: one outgoing message
-  static constexpr int kEnd0 = kPsOff + kMsgStride;       // 215040
+  static constexpr int kEnd0 = kPsOff + kMsgStride;       // 216064
   // rank 1
   static constexpr int kV8Off = 0;
-  static constexpr int kV16Off = kV8Off + kNV8 * kV8Stage;     // 65536
-  static constexpr int kPrOff = kV16Off + kNV16 * kV16Stage;   // 131072
-  static constexpr int kEnd1 = kPrOff + 2 * kMsgStride;        // 200704
+  static constexpr int kPrOff = kV8Off + kNV8 * kV8Stage;      // 131072
+  static constexpr int kEnd1 = kPrOff + 2 * kMsgStride;        // 202752
   static constexpr int kBarOff = kEnd0 > kEnd1 ? kEnd0 : kEnd1;
   static constexpr int kTotal = kBarOff + 512 + 1024;
 };
 static_assert(Fp8Smem::kTotal <= 232448, "shared memory budget");
-static_assert(Fp8Smem::kTile == 2 * Fp8Smem::kV8Sub && Fp8Smem::kV8Sub == 2 * Fp8Smem::kV16Sub,
-              "a tile is two E4M3 V stages, each two fp16 V stages");
+static_assert(Fp8Smem::kTile == 2 * Fp8Smem::kV8Sub, "a tile is two E4M3 V stages");
 
 enum : int {
   F_KFULL = 0,
@@ -90,15 +98,14 @@ enum : int {
   F_MSG_FREE = F_MMA_DONE_A + 1,  // rank 0: the outgoing P message has landed in rank 1
   F_V8FULL = F_MSG_FREE + 1,
   F_V8EMPTY = F_V8FULL + Fp8Smem::kNV8,
-  F_V16FULL = F_V8EMPTY + Fp8Smem::kNV8,
-  F_V16EMPTY = F_V16FULL + Fp8Smem::kNV16,
-  F_P_FULL = F_V16EMPTY + Fp8Smem::kNV16,   // 2
+  F_P_FULL = F_V8EMPTY + Fp8Smem::kNV8,     // 2
   F_PV_DONE = F_P_FULL + 2,       // 2
   F_META_READ = F_PV_DONE + 2,    // 2
   F_O_EMPTY = F_META_READ + 2,
   F_O_FIXED = F_O_EMPTY + 1,
   F_MMA_DONE_B = F_O_FIXED + 1,
-  F_COUNT = F_MMA_DONE_B + 1
+  F_P8_READY = F_MMA_DONE_B + 1,  // 2: a landed P' is in its E4M3 form
+  F_COUNT = F_P8_READY + 2
 };
 // barriers + TMEM slot + abort flag + 4 warp flags + the P message count
 static_assert((F_COUNT + 9) * 8 <= 512, "barrier block");
@@ -107,6 +114,25 @@ static_assert((F_COUNT + 9) * 8 <= 512, "barrier block");
 // a in the low byte.
 __device__ __forceinline__ uint32_t to_e4m3x2(float a, float b) {
   return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+// P' = 2^kPShift p: the lazy-rescale threshold keeps p <= 2^kRescaleThresh,
+// so p' <= 2^8 (inside E4M3's 448).
+constexpr float kRescaleThresh = 2.0f;
+constexpr int kPShift = 8 - 2;
+
+
+// Two fp16 p' values -> their E4M3 hi bytes and lo bytes (low element in the
+// low byte of each): hi = rn(p'), lo = rn(p' - hi); the remainder is exact in
+// fp16 (p' and hi share a binade, hi has 4 significant bits).
+__device__ __forceinline__ void split_e4m3x2(uint32_t p2, uint32_t& hi, uint32_t& lo) {
+  __half2_raw pr;
+  pr.x = static_cast<unsigned short>(p2 & 0xFFFFu);
+  pr.y = static_cast<unsigned short>(p2 >> 16);
+  hi = __nv_cvt_halfraw2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3);
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(hi), __NV_E4M3);
+  const __half2 rem = __hsub2(*reinterpret_cast<const __half2*>(&pr), *reinterpret_cast<const __half2*>(&hr));
+  lo = __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&rem), __NV_SATFINITE, __NV_E4M3);
 }
 
 // Two E4M3 bytes (the low one first) -> fp16x2, exact.
@@ -152,10 +178,100 @@ __device__ __forceinline__ float amax8(uint4 x, float m) {
   return m;
 }
 
+// Query row r of a new query token -> its two E4M3 terms: the latent part
+// into TMEM (hi at column t_hi, lo at t_lo, 4 bytes per column), the RoPE
+// part into row r of the 128-byte-swizzled sQr tile (hi bytes in units 0..3,
+// lo bytes in units 4..7).  The row's 16-bit chunks (8 latent, then RoPE)
+// are chunks 0..4 of ring stage st0 and 0..3 of st1.  Returns the row's
+// score factor scale_log2 * sq.  Out of line: it runs once per query token,
+// and the softmax loop it belongs to stays small.
+template <bool BF16>
+__device__ __noinline__ float quantize_query_row(const uint8_t* st0, const uint8_t* st1, int r,
+                                                 bool live, uint32_t t_hi, uint32_t t_lo,
+                                                 uint8_t* sQr, float scale_log2) {
+  auto qrow_ptr = [&](int c) -> const uint8_t* {
+    return (c < 5 ? st0 + c * Fp8Smem::kChunk : st1 + (c - 5) * Fp8Smem::kChunk) + r * 128;
+  };
+  float amax = 0.f;
+  for (int c = 0; c < 9; ++c) {
+    const uint8_t* rowp = qrow_ptr(c);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      amax = amax8<BF16>(*reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4)), amax);
+  }
+  if (!live) amax = 0.f;
+  // row scale sq = 2^(E - 8) with amax = f * 2^E, f in [0.5, 1): the row's
+  // largest value maps into [128, 256)
+  int E = 0;
+  frexpf(amax, &E);
+  const float inv_sq = live && amax > 0.f ? ldexpf(1.f, 8 - E) : 0.f;
+  for (int c = 0; c < 9; ++c) {
+    const uint8_t* rowp = qrow_ptr(c);
+    uint32_t hi[16], lo[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t h2[2], l2[2];
+      quantize8<BF16>(*reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4)), inv_sq, h2, l2);
+      hi[2 * j] = h2[0];
+      hi[2 * j + 1] = h2[1];
+      lo[2 * j] = l2[0];
+      lo[2 * j + 1] = l2[1];
+    }
+    if (c < 8) {
+      // 64 values = 16 columns of 4 bytes
+      tmem_st16(t_hi + c * 16, hi);
+      tmem_st16(t_lo + c * 16, lo);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        *reinterpret_cast<uint4*>(sQr + sw128_offset(r, u)) =
+            make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
+        *reinterpret_cast<uint4*>(sQr + sw128_offset(r, 4 + u)) =
+            make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
+      }
+    }
+  }
+  return scale_log2 * (amax > 0.f ? ldexpf(1.f, E - 8) : 1.f);
+}
+
+// O *= alpha on columns [cbeg, cbeg + 256) of this thread's TMEM row.
+// (This and store_o_half stay inline: as out-of-line functions called from
+// more than one site, their warp-collective TMEM loads returned zeros in one
+// template instance.)
+__device__ __forceinline__ void rescale_o(uint32_t trow, int cbeg, float alpha) {
+  for (int c0 = cbeg; c0 < cbeg + 256; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(trow + c0, v);
+    tmem_wait_ld(v);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
+    tmem_st32(trow + c0, v);
+  }
+  tmem_wait_st();
+}
+
+// Columns [cbeg, cbeg + 256) of this thread's TMEM row, times mul, stored as
+// 256 values of dtype dt at element e0 of dst.
+__device__ __forceinline__ void store_o_half(uint32_t trow, int cbeg, void* dst, int64_t e0, float mul,
+                                          int dt, bool active) {
+  for (int c0 = cbeg; c0 < cbeg + 256; c0 += 64) {
+    uint32_t v0[32], v1[32];
+    tmem_ld32(trow + c0, v0);
+    tmem_ld32(trow + c0 + 32, v1);
+    tmem_wait_ld(v0, v1);
+    if (active) {
+      store_row32(dst, e0 + c0, v0, mul, dt);
+      store_row32(dst, e0 + c0 + 32, v1, mul, dt);
+    }
+  }
+}
+
 }  // namespace
 
+constexpr int kFp8Threads = 384;
+
 template <bool BF16>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
     mla_partial_fp8_kernel(const __grid_constant__ CUtensorMap tm_qlat,
                            const __grid_constant__ CUtensorMap tm_qpe,
                            const __grid_constant__ CUtensorMap tm_kv,
@@ -168,7 +284,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   constexpr uint32_t kQhiCol = 0;        // rank 0: query hi bytes, 128 columns (4 per column)
   constexpr uint32_t kQloCol = 128;      // rank 0: query lo bytes, 128 columns
   constexpr uint32_t kSCol = 256;        // rank 0: S buffers [256,384), [384,512)
-  constexpr float kRescaleThresh = 8.0f; // lazy rescale: only when max grows by > 2^8
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -177,6 +292,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + F_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + F_COUNT + 1);
   volatile uint32_t* warp_flags = reinterpret_cast<volatile uint32_t*>(bar + F_COUNT + 2);
+  // rank 0: the softmax groups' row maxima of a tile and group A's row factors
+  __shared__ float s_rowmax[2][128];
+  __shared__ float s_fs[128];
   // rank 0: P messages sent; rank 1: P messages the watcher has seen land
   volatile int* msg_count = reinterpret_cast<volatile int*>(bar + F_COUNT + 8);
 
@@ -195,7 +313,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       mbar_init(&bar[F_QLAT_FULL], 4);
       for (int k = 0; k < 2; ++k) {
         mbar_init(&bar[F_S_FULL + k], 1);
-        mbar_init(&bar[F_S_EMPTY + k], 4);
+        mbar_init(&bar[F_S_EMPTY + k], 8);
         mbar_init(&bar[F_PFREE + k], 1);
       }
       mbar_init(&bar[F_MMA_DONE_A], 1);
@@ -203,20 +321,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     } else {
       for (int s = 0; s < L::kNV8; ++s) {
         mbar_init(&bar[F_V8FULL + s], 1);
-        mbar_init(&bar[F_V8EMPTY + s], 4);
-      }
-      for (int s = 0; s < L::kNV16; ++s) {
-        mbar_init(&bar[F_V16FULL + s], 4);
-        mbar_init(&bar[F_V16EMPTY + s], 1);
+        mbar_init(&bar[F_V8EMPTY + s], 1);
       }
       for (int k = 0; k < 2; ++k) {
         mbar_init(&bar[F_P_FULL + k], 1);
         mbar_init(&bar[F_PV_DONE + k], 1);
-        mbar_init(&bar[F_META_READ + k], 4);
+        mbar_init(&bar[F_META_READ + k], 8);
       }
-      mbar_init(&bar[F_O_EMPTY], 4);
-      mbar_init(&bar[F_O_FIXED], 4);
+      mbar_init(&bar[F_O_EMPTY], 8);
+      mbar_init(&bar[F_O_FIXED], 8);
       mbar_init(&bar[F_MMA_DONE_B], 1);
+      mbar_init(&bar[F_P8_READY + 0], 8);
+      mbar_init(&bar[F_P8_READY + 1], 8);
       // the first two P messages may land as soon as the cluster is up
       mbar_arrive_expect_tx(&bar[F_P_FULL + 0], L::kMsgBytes);
       mbar_arrive_expect_tx(&bar[F_P_FULL + 1], L::kMsgBytes);
@@ -250,7 +366,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   TileRange rng;
   Shares shares;
   bool split = false;
-  partition_tiles<TILE>(pp, cid, ncl, rng, shares, split);
+  partition_tiles<TILE, kFp8Threads>(pp, cid, ncl, rng, shares, split);
 
   const Waits waits{pp.spin_limit, abort_flag, err};
   auto wait = [&](uint64_t* b, uint32_t parity) { return waits.wait(b, parity); };
@@ -393,7 +509,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       }
     } else {
       // ------------------------------------------------ rank 0: query terms + softmax
-      const int r = threadIdx.x - 128;           // TMEM lane == head row
+      // Group A (w4-7) alone turns each new query into its E4M3 terms (named
+      // barrier 2); both groups (named barrier 1, 256 threads) then share the
+      // tiles' softmax by columns.  Every exit decision is made together
+      // through named_bar_and.
+      const int grp = warp >= 8 ? 1 : 0;
+      const int r = (threadIdx.x - 128) & 127;   // TMEM lane == head row
       const int wq = warp & 3;
       const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
       const uint32_t precv_peer = map_to_peer(smem + L::kPrOff, 1);
@@ -407,125 +528,74 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       bool ok = true;
       while (ok && it.valid) {
         const UnitInfo ui = it.ui;
+        bool qok = true;
         if (it.first()) {
-          if (it.newq) {
-            // (the softmax warps meet at named barriers, so every exit
-            // decision is made together through named_bar_and)
+          if (it.newq && grp == 0) {
             const bool qe = it.nq < 1 || wait_lazy(&bar[F_Q_EMPTY], (it.nq - 1) & 1);
             const bool q0 = qe && wait_lazy(&bar[F_KFULL + cq % L::kNK], (cq / L::kNK) & 1);
             const bool q1 =
                 q0 && wait_lazy(&bar[F_KFULL + (cq + 1) % L::kNK], ((cq + 1) / L::kNK) & 1);
-            if (!named_bar_and(1, 128, q1)) { ok = false; break; }
+            qok = named_bar_and(2, 128, q1);
+          }
+          if (it.newq && grp == 0 && qok) {
             tc_fence_after();
-            // row r of 16-bit chunk c (8 latent, then RoPE) in the ring:
-            // 16-byte unit j at (j ^ (r & 7))
-            auto qrow_ptr = [&](int c) -> const uint8_t* {
-              const int qs = c / 5, k = c % 5;
-              return sK + ((cq + qs) % L::kNK) * L::kKStage + k * L::kChunk + r * 128;
-            };
-            const bool live = r < pp.H;   // rows past H hold the next query's rows
-            float amax = 0.f;
-            for (int c = 0; c < 9; ++c) {
-              const uint8_t* rowp = qrow_ptr(c);
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                amax = amax8<BF16>(*reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4)),
-                                   amax);
-            }
-            if (!live) amax = 0.f;
-            // row scale sq = 2^(E - 8) with amax = f * 2^E, f in [0.5, 1):
-            // the row's largest value maps into [128, 256)
-            int E = 0;
-            frexpf(amax, &E);
-            const float inv_sq = live && amax > 0.f ? ldexpf(1.f, 8 - E) : 0.f;
-            fs = pp.scale_log2 * (amax > 0.f ? ldexpf(1.f, E - 8) : 1.f);
-            for (int c = 0; c < 8; ++c) {
-              const uint8_t* rowp = qrow_ptr(c);
-              uint32_t hi[16], lo[16];
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                uint32_t h2[2], l2[2];
-                quantize8<BF16>(*reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4)),
-                                inv_sq, h2, l2);
-                hi[2 * j] = h2[0];
-                hi[2 * j + 1] = h2[1];
-                lo[2 * j] = l2[0];
-                lo[2 * j + 1] = l2[1];
-              }
-              // 64 values = 16 columns of 4 bytes
-              tmem_st16(tmem + lane_base + kQhiCol + c * 16, hi);
-              tmem_st16(tmem + lane_base + kQloCol + c * 16, lo);
-            }
-            {
-              // RoPE row: hi bytes -> units 0..3, lo bytes -> units 4..7 of
-              // row r of the 128-byte-swizzled sQr tile
-              const uint8_t* rowp = qrow_ptr(8);
-              uint32_t hi[16], lo[16];
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                uint32_t h2[2], l2[2];
-                quantize8<BF16>(*reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4)),
-                                inv_sq, h2, l2);
-                hi[2 * j] = h2[0];
-                hi[2 * j + 1] = h2[1];
-                lo[2 * j] = l2[0];
-                lo[2 * j + 1] = l2[1];
-              }
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                *reinterpret_cast<uint4*>(sQr + sw128_offset(r, u)) =
-                    make_uint4(hi[4 * u], hi[4 * u + 1], hi[4 * u + 2], hi[4 * u + 3]);
-                *reinterpret_cast<uint4*>(sQr + sw128_offset(r, 4 + u)) =
-                    make_uint4(lo[4 * u], lo[4 * u + 1], lo[4 * u + 2], lo[4 * u + 3]);
-              }
-            }
+            // (rows past H hold the next query's rows: zero terms)
+            fs = quantize_query_row<BF16>(sK + (cq % L::kNK) * L::kKStage,
+                                          sK + ((cq + 1) % L::kNK) * L::kKStage, r, r < pp.H,
+                                          tmem + lane_base + kQhiCol, tmem + lane_base + kQloCol,
+                                          sQr, pp.scale_log2);
+            s_fs[r] = fs;   // group B's copy, read after the next joint barrier
             fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
-            named_bar_sync(1, 128);   // every row has read the query's ring stages
+            named_bar_sync(2, 128);   // every row has read the query's ring stages
             if (threadIdx.x == 128) {
               mbar_arrive(&bar[F_KEMPTY + cq % L::kNK]);
               mbar_arrive(&bar[F_KEMPTY + (cq + 1) % L::kNK]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[F_QLAT_FULL]);
-            cq += L::kQStages;
           }
+          if (it.newq) cq += L::kQStages;
           m = -INFINITY;
           l = 0.f;
         }
         const int sb = g & 1;
-        if (!named_bar_and(1, 128, wait_lazy(&bar[F_S_FULL + sb], (g >> 1) & 1))) {
+        if (!named_bar_and(1, 256, qok && wait_lazy(&bar[F_S_FULL + sb], (g >> 1) & 1))) {
           ok = false;
           break;
         }
+        if (it.first() && it.newq && grp == 1) fs = s_fs[r];
         tc_fence_after();
-        float s[TILE];
-        // S in four 32-column loads, each folded into the row max before the
-        // next is issued
-        const int nvalid = min(TILE, ui.hi - (ui.lo + it.j * TILE));
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // this group's columns [c0, c0 + 64) of the tile: one TMEM read (two
+        // loads, one wait), after which the S buffer goes back to the MMA
+        const int c0 = 64 * grp;
+        const int nvalid = min(TILE, ui.hi - (ui.lo + it.j * TILE)) - c0;
+        const uint32_t sa = tmem + lane_base + kSCol + sb * TILE + c0;
+        uint32_t v[64];
         {
-          const uint32_t sa = tmem + lane_base + kSCol + sb * TILE;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            tmem_ld32(sa + 32 * c, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int t = 0; t < 32; ++t) {
-              const int tt = 32 * c + t;
-              s[tt] = tt < nvalid ? __uint_as_float(v[t]) * fs : -INFINITY;
-              mx[t & 3] = fmaxf(mx[t & 3], s[tt]);
-            }
-          }
+          uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(v);
+          uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 32);
+          tmem_ld32(sa, v0);
+          tmem_ld32(sa + 32, v1);
+          tmem_wait_ld(v0, v1);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[F_S_EMPTY + sb]);
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int t = 0; t < 64; ++t)
+          if (t < nvalid) mx[t & 3] = fmaxf(mx[t & 3], __uint_as_float(v[t]));
+        s_rowmax[grp][r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        // the P message buffer is free once rank 1 reports the previous
+        // message landed (F_MSG_FREE); one barrier also exchanges the maxima
+        bool mfree = true;
+        if (threadIdx.x == 128 && g >= 1) mfree = wait_cl(&bar[F_MSG_FREE], (g - 1) & 1);
+        if (!named_bar_and(1, 256, mfree)) { ok = false; break; }
+        const float mt = fmaxf(s_rowmax[0][r], s_rowmax[1][r]) * fs;   // fs > 0
 
         // ---- online softmax in the log2 domain
-        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         bool need_rescale = false;
         float alpha = 1.f;
         if (it.first()) {
@@ -535,39 +605,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           alpha = fast_exp2(m - mt);
           m = mt;
         }
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int t = 0; t < TILE; ++t) {
-          s[t] = fast_exp2(s[t] - m);     // masked: exp2(-inf) = 0
-          ps[t & 3] += s[t];
-        }
-        l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
 
-        // ---- P message for rank 1 (fp16 P; single outgoing buffer, free once
-        // rank 1 reports the previous message landed on F_MSG_FREE)
-        uint8_t* msg = sPs;
-        bool mfree = true;
-        if (threadIdx.x == 128 && g >= 1) mfree = wait_cl(&bar[F_MSG_FREE], (g - 1) & 1);
-        if (!named_bar_and(1, 128, mfree)) { ok = false; break; }
+        // ---- P message for rank 1: p' = 2^6 exp2(s - m) in fp16, this
+        // group's 64 tokens = its 16 KB tile of the message
+        uint8_t* msg = sPs + grp * 16384;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        const float mp = static_cast<float>(kPShift) - m;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int uu = 0; uu < 8; ++uu) {
+          float p[8];
 #pragma unroll
-          for (int uu = 0; uu < 8; ++uu) {
-            const int t = half * 64 + uu * 8;
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) w[e] = pack2<false>(s[t + 2 * e], s[t + 2 * e + 1]);
-            *reinterpret_cast<uint4*>(msg + half * 16384 + sw128_offset(r, uu)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
+          for (int e = 0; e < 8; ++e) {
+            const int t = 8 * uu + e;
+            // masked columns: 0; others p' <= 2^8
+            p[e] = t < nvalid ? fast_exp2(fmaf(__uint_as_float(v[t]), fs, mp)) : 0.f;
+            ps[e & 3] += p[e];
           }
+          *reinterpret_cast<uint4*>(msg + sw128_offset(r, uu)) =
+              make_uint4(pack2<false>(p[0], p[1]), pack2<false>(p[2], p[3]),
+                         pack2<false>(p[4], p[5]), pack2<false>(p[6], p[7]));
         }
-        reinterpret_cast<float*>(msg + L::kMsgAlpha)[r] = alpha;
-        reinterpret_cast<float*>(msg + L::kMsgL)[r] = l;
-        reinterpret_cast<float*>(msg + L::kMsgM)[r] = m;
-        const uint32_t any = __any_sync(0xffffffffu, need_rescale) ? 1u : 0u;
-        if (lane == 0) warp_flags[wq] = any;
+        l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));   // this group's half of the row sum of p'
+        msg = sPs;
+        if (grp == 0) {
+          reinterpret_cast<float*>(msg + L::kMsgAlpha)[r] = alpha;
+          reinterpret_cast<float*>(msg + L::kMsgLA)[r] = l;
+          reinterpret_cast<float*>(msg + L::kMsgM)[r] = m;
+          // (both groups take the same rescale decisions: group A's flags)
+          const uint32_t any = __any_sync(0xffffffffu, need_rescale) ? 1u : 0u;
+          if (lane == 0) warp_flags[wq] = any;
+        } else {
+          reinterpret_cast<float*>(msg + L::kMsgLB)[r] = l;
+        }
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, 256);
         if (threadIdx.x == 128) {
           const uint32_t flags = (warp_flags[0] | warp_flags[1] | warp_flags[2] | warp_flags[3]) |
                                  (it.last() ? 2u : 0u);
@@ -580,7 +651,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             *msg_count = g + 1;
           }
         }
-        ok = named_bar_and(1, 128, ok && !*abort_flag);
+        ok = named_bar_and(1, 256, ok && !*abort_flag);
         it.advance(pp);
         ++g;
         cq += 1;
@@ -588,7 +659,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     }
   } else {
     uint8_t* sV8 = smem + L::kV8Off;
-    uint8_t* sV16 = smem + L::kV16Off;
     uint8_t* sPr = smem + L::kPrOff;
     if (warp == 0) {
       // ------------------------------------------------ rank 1: TMA producer (E4M3 V)
@@ -635,8 +705,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     } else if (warp == 1) {
       // ------------------------------------------------ rank 1: MMA issuer (PV)
       if (lane == 0) {
-        constexpr uint32_t idesc = make_idesc_f16(128, 256, false, false, true);   // fp16, V MN-major
-        const uint32_t v_base = smem_u32(sV16);
+        // E4M3 x E4M3 -> fp32; P K-major, V MN-major (latent-contiguous rows)
+        constexpr uint32_t idesc = make_idesc_f16(128, 256, false, false, true);
+        const uint32_t v_base = smem_u32(sV8);
         const uint32_t p_base = smem_u32(sPr);
         TileIter<TILE> it;
         it.start(pp, rng);
@@ -644,7 +715,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         bool ok = true;
         while (ok && it.valid) {
           const int sb = g & 1;
-          if (!wait(&bar[F_P_FULL + sb], (g >> 1) & 1)) break;
+          if (!wait(&bar[F_P8_READY + sb], (g >> 1) & 1)) break;
           const uint32_t hdr =
               *reinterpret_cast<volatile uint32_t*>(sPr + sb * L::kMsgStride + L::kMsgHdr);
           const bool first = it.first();
@@ -654,23 +725,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             ++nfix;
           }
           const uint32_t pa = p_base + sb * L::kMsgStride;
-          for (int sub = 0; sub < TILE / L::kV16Sub; ++sub) {
-            const int st = vs % L::kNV16;
-            if (!wait(&bar[F_V16FULL + st], (vs / L::kNV16) & 1)) { ok = false; break; }
+          for (int sub = 0; sub < TILE / L::kV8Sub; ++sub) {
+            const int st = vs % L::kNV8;
+            if (!wait(&bar[F_V8FULL + st], (vs / L::kNV8) & 1)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t vb = v_base + st * L::kV16Stage;
+            const uint32_t vb = v_base + st * L::kV8Stage;
 #pragma unroll
-            for (int kk = 0; kk < L::kV16Sub / 16; ++kk) {
-              const int tok = sub * L::kV16Sub + kk * 16;
-              const uint64_t ad = make_desc_sw128(pa + (tok >> 6) * 16384 + (tok & 63) * 2, 16, 1024);
+            for (int kk = 0; kk < L::kV8Sub / 32; ++kk) {
 #pragma unroll
-              for (int half = 0; half < 2; ++half) {
-                const uint64_t bd =
-                    make_desc_sw128(vb + half * 4 * L::kV16Chunk + kk * 2048, L::kV16Chunk, 1024);
-                umma_ss(tmem + half * 256, ad, bd, idesc, (first && sub == 0 && kk == 0) ? 0u : 1u);
+              for (int term = 0; term < 2; ++term) {
+                // tokens [64 sub + 32 kk, +32) of the hi (bytes 0..63) or lo
+                // (bytes 64..127) half of the rows of tile `sub`
+                const uint64_t ad = make_desc_sw128(pa + sub * 16384 + term * 64 + kk * 32, 16, 1024);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                  const uint64_t bd = make_desc_sw128(vb + half * 2 * L::kV8Chunk + kk * 32 * 128,
+                                                      L::kV8Chunk, 1024);
+                  umma_ss_f8(tmem + half * 256, ad, bd, idesc,
+                             (first && sub == 0 && kk == 0 && term == 0) ? 0u : 1u);
+                }
               }
             }
-            umma_commit(&bar[F_V16EMPTY + st]);
+            umma_commit(&bar[F_V8EMPTY + st]);
             ++vs;
           }
           if (!ok) break;
@@ -732,106 +808,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         }
       }
     } else {
-      // ------------------------------------------------ rank 1: V widening, O rescale, epilogue
-      const int r = threadIdx.x - 128;
+      // ------------------------------------------------ rank 1: O rescale + epilogue
+      // group A: latent columns [0, 256), group B: [256, 512) of row r
+      const int grp = warp >= 8 ? 1 : 0;
+      const int r = (threadIdx.x - 128) & 127;
       const int wq = warp & 3;
+      const int cbeg = 256 * grp;
       const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-      // V widening: warp wq takes tokens [8 wq, 8 wq + 8) of each 32-token
-      // fp16 stage, lane = (token t_in, 16-byte unit uu); per step one
-      // 64-latent group q: 8 tokens x 64 bytes read, 8 x 128 bytes written
-      // (both 128-byte-swizzled, so every access hits each bank 4 times).
-      // Tokens past the tile's valid ones (slots after the history's end in
-      // its last page, whatever bytes they hold) are written as zeros: their
-      // P is 0, and 0 times a NaN code would still be NaN.
-      const int t_in = lane >> 2, uu = lane & 3;
-      const int tv = 8 * wq + t_in;   // token within the fp16 stage
-      int v16 = 0;
-      auto widen = [&](bool live) -> bool {
-        const int s8 = v16 >> 1, h = v16 & 1;
-        const int st8 = s8 % L::kNV8, st16 = v16 % L::kNV16;
-        if (h == 0 && !wait_lazy(&bar[F_V8FULL + st8], (s8 / L::kNV8) & 1)) return false;
-        if (v16 >= L::kNV16 && !wait_lazy(&bar[F_V16EMPTY + st16], ((v16 / L::kNV16) - 1) & 1))
-          return false;
-        const uint8_t* src = sV8 + st8 * L::kV8Stage;
-        uint8_t* dst = sV16 + st16 * L::kV16Stage;
-        const int row8 = h * L::kV16Sub + tv;   // row within the E4M3 stage
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          // latent bytes [64 q + 16 uu, +16) of the token
-          uint4 x = *reinterpret_cast<const uint4*>(
-              src + (q >> 1) * L::kV8Chunk + sw128_offset(row8, (q & 1) * 4 + uu));
-          if (!live) x = make_uint4(0, 0, 0, 0);
-          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-          uint32_t f[8];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            f[2 * k] = e4m3x2_to_f16x2(w[k] & 0xFFFFu);
-            f[2 * k + 1] = e4m3x2_to_f16x2(w[k] >> 16);
-          }
-          uint8_t* o = dst + q * L::kV16Chunk;
-          *reinterpret_cast<uint4*>(o + sw128_offset(tv, 2 * uu)) = make_uint4(f[0], f[1], f[2], f[3]);
-          *reinterpret_cast<uint4*>(o + sw128_offset(tv, 2 * uu + 1)) =
-              make_uint4(f[4], f[5], f[6], f[7]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bar[F_V16FULL + st16]);
-          if (h == 1) mbar_arrive(&bar[F_V8EMPTY + st8]);
-        }
-        ++v16;
-        return true;
-      };
-      // Epilogue of a piece: O * (kv_scale / l) and its LSE, after the
-      // piece's last PV MMAs.  It runs once the next tile's first two fp16 V
-      // stages are written (those need only the previous tile's MMAs), so
-      // the V widening never waits on it.
-      struct Pending {
-        int64_t row_out;
-        int slot;
-        float lse2, mul;
-        int g;
-        bool whole, on;
-      } pend;
-      pend.on = false;
-      auto epilogue = [&]() -> bool {
-        if (!wait_lazy(&bar[F_PV_DONE + (pend.g & 1)], (pend.g >> 1) & 1)) return false;
-        tc_fence_after();
-        if (pend.whole) {
-          for (int c0 = 0; c0 < 512; c0 += 64) {
-            uint32_t v0[32], v1[32];
-            tmem_ld32(tmem + lane_base + c0, v0);
-            tmem_ld32(tmem + lane_base + c0 + 32, v1);
-            tmem_wait_ld();
-            if (r < pp.H) {
-              store_row32(pp.o_part, pend.row_out * 512 + c0, v0, pend.mul, pp.part_dtype);
-              store_row32(pp.o_part, pend.row_out * 512 + c0 + 32, v1, pend.mul, pp.part_dtype);
-            }
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar[F_O_EMPTY]);
-          if (r < pp.H) pp.lse_part[pend.row_out] = pend.lse2 * kLn2;
-        } else {
-          // a piece of a unit split across pairs: O / l and the LSE (log2)
-          // parked in this pair's workspace slot for the merge kernel
-          for (int c0 = 0; c0 < 512; c0 += 64) {
-            uint32_t v0[32], v1[32];
-            tmem_ld32(tmem + lane_base + c0, v0);
-            tmem_ld32(tmem + lane_base + c0 + 32, v1);
-            tmem_wait_ld();
-            const int64_t e = (static_cast<int64_t>(pend.slot) * 128 + r) * 512 + c0;
-            store_row32(pp.ws_o, e, v0, pend.mul, pp.part_dtype);
-            store_row32(pp.ws_o, e + 32, v1, pend.mul, pp.part_dtype);
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar[F_O_EMPTY]);
-          pp.ws_lse[pend.slot * 128 + r] = pend.lse2;
-        }
-        pend.on = false;
-        return true;
-      };
       TileIter<TILE> it;
       it.start(pp, rng);
       int g = 0;
@@ -839,58 +822,86 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       while (ok && it.valid) {
         const UnitInfo ui = it.ui;
         const int sb = g & 1;
-        const int nvalid = min(TILE, ui.hi - (ui.lo + it.j * TILE));
-        // (1) the tile's first two fp16 V stages (they need only the
-        // previous tile's MMAs to be done with their buffers)
-        if (!widen(tv < nvalid) || !widen(L::kV16Sub + tv < nvalid)) { ok = false; break; }
-        // (2) the epilogue of the piece that ended with the previous tile
-        if (pend.on && !epilogue()) { ok = false; break; }
-        // (3) this tile's message header
         if (!wait_lazy(&bar[F_P_FULL + sb], (g >> 1) & 1)) { ok = false; break; }
-        const uint8_t* msg = sPr + sb * L::kMsgStride;
+        uint8_t* msg = sPr + sb * L::kMsgStride;
         const uint32_t hdr = *reinterpret_cast<const volatile uint32_t*>(msg + L::kMsgHdr);
         const float alpha = reinterpret_cast<const float*>(msg + L::kMsgAlpha)[r];
-        const float lsum = reinterpret_cast<const float*>(msg + L::kMsgL)[r];
+        const float lsum = reinterpret_cast<const float*>(msg + L::kMsgLA)[r] +
+                           reinterpret_cast<const float*>(msg + L::kMsgLB)[r];
         const float m2 = reinterpret_cast<const float*>(msg + L::kMsgM)[r];
+        {
+          // row r of this group's 64 tokens: fp16 p' -> [hi bytes | lo bytes]
+          // in the same 128-byte row (each thread rewrites only its own row)
+          uint8_t* row = msg + grp * 16384;
+          uint4 x[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) x[u] = *reinterpret_cast<const uint4*>(row + sw128_offset(r, u));
+          uint32_t hw[16], lw[16];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+            uint32_t h[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split_e4m3x2(w[e], h[e], lo[e]);
+            hw[2 * u] = h[0] | (h[1] << 16);
+            hw[2 * u + 1] = h[2] | (h[3] << 16);
+            lw[2 * u] = lo[0] | (lo[1] << 16);
+            lw[2 * u + 1] = lo[2] | (lo[3] << 16);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            *reinterpret_cast<uint4*>(row + sw128_offset(r, u)) =
+                make_uint4(hw[4 * u], hw[4 * u + 1], hw[4 * u + 2], hw[4 * u + 3]);
+            *reinterpret_cast<uint4*>(row + sw128_offset(r, 4 + u)) =
+                make_uint4(lw[4 * u], lw[4 * u + 1], lw[4 * u + 2], lw[4 * u + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar[F_P8_READY + sb]);
+        }
+        // the message's header fields are in registers: the slot may go back
+        // (once the PV MMAs have read its P as well)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[F_META_READ + sb]);
-        // (4) O *= alpha before PV of this tile (never on a piece's first tile)
         if (hdr & 1u) {
+          // O *= alpha before PV of this tile; PV of the previous tile must be done
           if (!wait_lazy(&bar[F_PV_DONE + ((g - 1) & 1)], ((g - 1) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          for (int c0 = 0; c0 < 512; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + c0, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
-            tmem_st32(tmem + lane_base + c0, v);
-          }
-          tmem_wait_st();
+          rescale_o(tmem + lane_base, cbeg, alpha);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bar[F_O_FIXED]);
         }
-        // (5) the tile's other two fp16 V stages
-        if (!widen(2 * L::kV16Sub + tv < nvalid) || !widen(3 * L::kV16Sub + tv < nvalid)) {
-          ok = false;
-          break;
-        }
-        // (6) a piece ends with this tile: its epilogue follows the next
-        // tile's first V stages (or the loop)
         if (hdr & 2u) {
-          pend.on = true;
-          pend.g = g;
-          pend.lse2 = m2 + __log2f(lsum);
-          pend.mul = pp.out_scale / lsum;
-          pend.whole = it.whole();
-          pend.slot = 2 * cid + (it.u == rng.u_begin ? 0 : 1);
-          pend.row_out = part_row(pp, static_cast<int64_t>(ui.b) * pp.q_len + ui.i, ui.p, r);
+          // epilogue of the piece: O * kv_scale / (2^6 l) and its LSE
+          if (!wait_lazy(&bar[F_PV_DONE + sb], (g >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const float lse2 = m2 + __log2f(lsum) - static_cast<float>(kPShift);   // log2 domain
+          const float mul = pp.out_scale / lsum;   // lsum is the row sum of p' = 2^6 p
+          const int64_t row_out =
+              part_row(pp, static_cast<int64_t>(ui.b) * pp.q_len + ui.i, ui.p, r);   // r < H only
+          // whole unit: o_part rows; a piece of a unit split across pairs:
+          // O / l and the LSE (log2) parked in this pair's workspace slot for
+          // the merge kernel
+          const bool whole = it.whole();
+          const int slot = 2 * cid + (it.u == rng.u_begin ? 0 : 1);
+          if (whole)
+            store_o_half(tmem + lane_base, cbeg, pp.o_part, row_out * 512, mul, pp.part_dtype,
+                         r < pp.H);
+          else
+            store_o_half(tmem + lane_base, cbeg, pp.ws_o, (static_cast<int64_t>(slot) * 128 + r) * 512,
+                         mul, pp.part_dtype, true);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar[F_O_EMPTY]);
+          if (grp == 0) {
+            if (!whole) pp.ws_lse[slot * 128 + r] = lse2;
+            else if (r < pp.H) pp.lse_part[row_out] = lse2 * kLn2;
+          }
         }
         it.advance(pp);
         ++g;
       }
-      if (ok && pend.on) epilogue();
     }
   }
 
@@ -936,7 +947,7 @@ static int prepare_partial_fp8(int* clusters) {
       return -1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(kFp8Threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -968,7 +979,7 @@ static int launch_partial_fp8_t(const CUtensorMap& qlat, const CUtensorMap& qpe,
   if (prepare_partial_fp8<BF16>(&max_clusters) != 0) return -1;
   const int clusters = pp.split ? pp.split : std::max(1, std::min(pp.num_units, max_clusters));
   if (clusters > max_clusters) return -1;
-  mla_partial_fp8_kernel<BF16><<<dim3(2 * clusters), dim3(256), Fp8Smem::kTotal, stream>>>(
+  mla_partial_fp8_kernel<BF16><<<dim3(2 * clusters), dim3(kFp8Threads), Fp8Smem::kTotal, stream>>>(
       qlat, qpe, kv, cur, kv_v, cur_v, pp);
   return pp.split ? launch_partial_merge(pp, clusters, stream) : 0;
 }

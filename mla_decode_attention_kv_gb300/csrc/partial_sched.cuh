@@ -21,8 +21,11 @@ struct UnitInfo {
   int ntiles;
 };
 
+// (out of line: it is called from every role's tile iterator, rarely on the
+// per-tile path, and its inlined copies would spread the kernels' hot loops
+// over more instruction-cache lines)
 template <int TILE>
-__device__ __forceinline__ UnitInfo unit_info(const PartialParams& pp, int u) {
+__device__ __noinline__ UnitInfo unit_info(const PartialParams& pp, int u) {
   UnitInfo ui;
   ui.p = u % pp.P;
   const int bi = u / pp.P;
@@ -153,11 +156,14 @@ struct Shares {
 // are merged through the workspace); without one the pair owns the whole
 // units whose first tile falls in its share.  Units without tiles (o = 0,
 // lse = -inf) are dealt round-robin elsewhere: unit u to pair u mod pairs.
-// Both CTAs of a pair compute the same range.  Called by all 256 threads.
-template <int TILE>
+// Both CTAs of a pair compute the same range.  Called by all NT threads of
+// the CTA (a multiple of 32, at most 512; at most 256 pairs).
+template <int TILE, int NT>
 __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid, int ncl,
                                                 TileRange& rng, Shares& sh, bool& split) {
-  __shared__ int s_scan[8];
+  static_assert(NT % 32 == 0 && NT <= 512, "block size");
+  constexpr int kWarps = NT / 32;
+  __shared__ int s_scan[kWarps];
   __shared__ int s_load[256];
   __shared__ int s_rng[4];
   const int warp = threadIdx.x >> 5;
@@ -166,7 +172,7 @@ __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid
   sh.ncl = ncl;
   split = false;
   const int U = pp.num_units;
-  const int per = (U + 255) / 256;
+  const int per = (U + NT - 1) / NT;
   const int a = min(U, static_cast<int>(threadIdx.x) * per);
   const int e = min(U, a + per);
   int cnt = 0;
@@ -185,11 +191,11 @@ __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid
     s_rng[2] = -1;        // u_last
     s_rng[3] = 0;         // j_stop
   }
-  for (int c = threadIdx.x; c < ncl; c += 256) s_load[c] = 0;
+  for (int c = threadIdx.x; c < ncl; c += NT) s_load[c] = 0;
   __syncthreads();
   int warp_base = 0, all = 0;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) {
+  for (int w = 0; w < kWarps; ++w) {
     const int t = s_scan[w];
     warp_base += w < warp ? t : 0;
     all += t;
@@ -208,7 +214,7 @@ __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid
     }
     __syncthreads();
     int mx = 0;
-    for (int c = threadIdx.x; c < ncl; c += 256) mx = max(mx, s_load[c]);
+    for (int c = threadIdx.x; c < ncl; c += NT) mx = max(mx, s_load[c]);
     const int64_t even = (sh.total + ncl - 1) / ncl;
     // any pair above the threshold decides for all
     split = __syncthreads_or(mx > even + max(int64_t{2}, even / 8)) != 0;
@@ -267,36 +273,57 @@ __device__ __forceinline__ void record_split_unit(const PartialParams& pp, int c
 // flag raised by another warp gives up too.  (The drains at the end of a
 // kernel, which wait for copies and MMAs already issued, use mbar_wait with
 // the fixed kSpinLimit: those always complete.)
+// The polling loops are out of line: a wait that is already satisfied costs
+// one try_wait at the call site, and the many call sites of the pipelines do
+// not each carry a copy of the loop (the kernels' per-tile code then stays
+// small enough for the instruction cache).
+static __device__ __noinline__ bool wait_spin_slow(uint64_t* b, uint32_t parity, uint32_t limit,
+                                            volatile int* abort_flag, int* err) {
+  for (uint32_t it = 0; it < limit; ++it) {
+    if (mbar_try_wait(b, parity)) return true;
+    if ((it & 1023u) == 1023u && *abort_flag) return false;
+  }
+  set_error(err, kDevWaitTimeout);
+  *abort_flag = 1;
+  return false;
+}
+
+static __device__ __noinline__ bool wait_lazy_slow(uint64_t* b, uint32_t parity, uint32_t limit,
+                                            volatile int* abort_flag, int* err) {
+  for (uint32_t it = 0; it < limit; ++it) {
+    if (mbar_try_wait_sleep(b, parity, kLazyWaitNs)) return true;
+    if ((it & 15u) == 15u && *abort_flag) return false;
+  }
+  set_error(err, kDevWaitTimeout);
+  *abort_flag = 1;
+  return false;
+}
+
+static __device__ __noinline__ bool wait_cluster_slow(uint64_t* b, uint32_t parity, uint32_t limit,
+                                               volatile int* abort_flag, int* err) {
+  for (uint32_t it = 0; it < limit; ++it) {
+    if (mbar_try_wait_cluster(b, parity)) return true;
+    if ((it & 1023u) == 1023u && *abort_flag) return false;
+  }
+  set_error(err, kDevWaitTimeout);
+  *abort_flag = 1;
+  return false;
+}
+
 struct Waits {
   uint32_t limit;
   volatile int* abort_flag;
   int* err;
-  __device__ __forceinline__ bool fail() const {
-    set_error(err, kDevWaitTimeout);
-    *abort_flag = 1;
-    return false;
-  }
   __device__ __forceinline__ bool wait(uint64_t* b, uint32_t parity) const {
-    for (uint32_t it = 0; it < limit; ++it) {
-      if (mbar_try_wait(b, parity)) return true;
-      if ((it & 1023u) == 1023u && *abort_flag) return false;
-    }
-    return fail();
+    return mbar_try_wait(b, parity) || wait_spin_slow(b, parity, limit, abort_flag, err);
   }
   // waits of whole warp groups off the issue path: polls may suspend
   __device__ __forceinline__ bool lazy(uint64_t* b, uint32_t parity) const {
-    for (uint32_t it = 0; it < limit; ++it) {
-      if (mbar_try_wait_sleep(b, parity, kLazyWaitNs)) return true;
-      if ((it & 15u) == 15u && *abort_flag) return false;
-    }
-    return fail();
+    return mbar_try_wait(b, parity) || wait_lazy_slow(b, parity, limit, abort_flag, err);
   }
   __device__ __forceinline__ bool cluster(uint64_t* b, uint32_t parity) const {
-    for (uint32_t it = 0; it < limit; ++it) {
-      if (mbar_try_wait_cluster(b, parity)) return true;
-      if ((it & 1023u) == 1023u && *abort_flag) return false;
-    }
-    return fail();
+    return mbar_try_wait_cluster(b, parity) ||
+           wait_cluster_slow(b, parity, limit, abort_flag, err);
   }
 };
 

@@ -110,8 +110,9 @@ def test_fp8_edge_lengths(lens):
     _check_split(dp, o_part, lse_part)
 
 
-def test_fp8_nan_bytes_past_the_history_are_ignored():
-    """Slots of a last page past L_b may hold any bytes, the NaN codes too."""
+def test_fp8_stale_bytes_past_the_history_are_ignored():
+    """Slots of a last page past L_b may hold any finite codes (stale tokens,
+    values up to +-448): they get weight 0."""
     cfg = inputs.DecodeConfig(name="fn", batch=3, heads=128, q_len=1, num_shards=2,
                               block_size=64, history=1, kv_scale=2.0 ** -8, seed=132, **F8)
     lens = np.array([70, 129, 5], np.int32)
@@ -119,7 +120,8 @@ def test_fp8_nan_bytes_past_the_history_are_ignored():
     for b in range(cfg.batch):
         L = int(lens[b])
         last = prob.block_table[b, (L - 1) // cfg.block_size]
-        prob.kv_cache[last, L % cfg.block_size or cfg.block_size:, :] = 0x7F
+        tail = prob.kv_cache[last, L % cfg.block_size or cfg.block_size:, :]
+        tail[:] = np.where(np.arange(tail.size).reshape(tail.shape) % 2, 0x7E, 0xFE)
     dp = DeviceProblem(prob)
     o_part, lse_part = dp.partial()
     torch.cuda.synchronize()
