@@ -35,7 +35,7 @@
 //           groups run the softmax of a tile, A on its columns 0..63 and B
 //           on 64..127 (the row max is exchanged through shared memory)
 //   rank 1: w0 TMA producer (E4M3 V), w1 MMA issuer, w2 hands P buffers
-//           back, w3 zeros of empty parts + P landing watcher; groups A / B
+//           back, w3 zeros of empty parts; groups A / B
 //           rescale O and write the epilogue of latent columns 0..255 /
 //           256..511
 // Every wait is bounded, as in the 16-bit kernel.
@@ -74,8 +74,9 @@ struct Fp8Smem {
   // rank 0
   static constexpr int kKOff = 0;
   static constexpr int kQr8Off = kKOff + kNK * kKStage;   // 163840: query RoPE, hi | lo bytes
-  static constexpr int kPsOff = kQr8Off + 16384;          // 180224: one outgoing message
-  static constexpr int kEnd0 = kPsOff + kMsgStride;       // 216064
+  static constexpr int kEnd0 = kQr8Off + 16384;           // 180224
+  // (rank 0 has no message buffer: its softmax threads write each P message
+  // straight into rank 1's landing slot with st.async)
   // rank 1
   static constexpr int kV8Off = 0;
   static constexpr int kPrOff = kV8Off + kNV8 * kV8Stage;      // 131072
@@ -95,8 +96,7 @@ enum : int {
   F_S_EMPTY = F_S_FULL + 2,       // 2
   F_PFREE = F_S_EMPTY + 2,        // 2
   F_MMA_DONE_A = F_PFREE + 2,
-  F_MSG_FREE = F_MMA_DONE_A + 1,  // rank 0: the outgoing P message has landed in rank 1
-  F_V8FULL = F_MSG_FREE + 1,
+  F_V8FULL = F_MMA_DONE_A + 1,
   F_V8EMPTY = F_V8FULL + Fp8Smem::kNV8,
   F_P_FULL = F_V8EMPTY + Fp8Smem::kNV8,     // 2
   F_PV_DONE = F_P_FULL + 2,       // 2
@@ -234,12 +234,13 @@ __device__ __noinline__ float quantize_query_row(const uint8_t* st0, const uint8
   return scale_log2 * (amax > 0.f ? ldexpf(1.f, E - 8) : 1.f);
 }
 
-// O *= alpha on columns [cbeg, cbeg + 256) of this thread's TMEM row.
+// O *= alpha on columns [cbeg, cbeg + NC) of this thread's TMEM row.
 // (This and store_o_half stay inline: as out-of-line functions called from
 // more than one site, their warp-collective TMEM loads returned zeros in one
 // template instance.)
+template <int NC>
 __device__ __forceinline__ void rescale_o(uint32_t trow, int cbeg, float alpha) {
-  for (int c0 = cbeg; c0 < cbeg + 256; c0 += 32) {
+  for (int c0 = cbeg; c0 < cbeg + NC; c0 += 32) {
     uint32_t v[32];
     tmem_ld32(trow + c0, v);
     tmem_wait_ld(v);
@@ -250,11 +251,12 @@ __device__ __forceinline__ void rescale_o(uint32_t trow, int cbeg, float alpha) 
   tmem_wait_st();
 }
 
-// Columns [cbeg, cbeg + 256) of this thread's TMEM row, times mul, stored as
-// 256 values of dtype dt at element e0 of dst.
+// Columns [cbeg, cbeg + NC) of this thread's TMEM row, times mul, stored as
+// NC values of dtype dt at element e0 + cbeg of dst.
+template <int NC>
 __device__ __forceinline__ void store_o_half(uint32_t trow, int cbeg, void* dst, int64_t e0, float mul,
                                           int dt, bool active) {
-  for (int c0 = cbeg; c0 < cbeg + 256; c0 += 64) {
+  for (int c0 = cbeg; c0 < cbeg + NC; c0 += 64) {
     uint32_t v0[32], v1[32];
     tmem_ld32(trow + c0, v0);
     tmem_ld32(trow + c0 + 32, v1);
@@ -268,7 +270,12 @@ __device__ __forceinline__ void store_o_half(uint32_t trow, int cbeg, void* dst,
 
 }  // namespace
 
-constexpr int kFp8Threads = 384;
+// Warp groups (4 warps each) that share a tile's softmax on rank 0 (by
+// columns) and O's rescale / epilogue on rank 1 (by latent columns).
+constexpr int kGroups = 2;
+constexpr int kFp8Threads = 128 + 128 * kGroups;
+constexpr int kSCols = 128 / kGroups;    // S columns (tokens) per softmax thread
+constexpr int kOCols = 512 / kGroups;    // O columns per epilogue thread
 
 template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
@@ -293,7 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + F_COUNT + 1);
   volatile uint32_t* warp_flags = reinterpret_cast<volatile uint32_t*>(bar + F_COUNT + 2);
   // rank 0: the softmax groups' row maxima of a tile and group A's row factors
-  __shared__ float s_rowmax[2][128];
+  __shared__ float s_rowmax[kGroups][128];
   __shared__ float s_fs[128];
   // rank 0: P messages sent; rank 1: P messages the watcher has seen land
   volatile int* msg_count = reinterpret_cast<volatile int*>(bar + F_COUNT + 8);
@@ -313,11 +320,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
       mbar_init(&bar[F_QLAT_FULL], 4);
       for (int k = 0; k < 2; ++k) {
         mbar_init(&bar[F_S_FULL + k], 1);
-        mbar_init(&bar[F_S_EMPTY + k], 8);
+        mbar_init(&bar[F_S_EMPTY + k], 4 * kGroups);
         mbar_init(&bar[F_PFREE + k], 1);
       }
       mbar_init(&bar[F_MMA_DONE_A], 1);
-      mbar_init(&bar[F_MSG_FREE], 1);
     } else {
       for (int s = 0; s < L::kNV8; ++s) {
         mbar_init(&bar[F_V8FULL + s], 1);
@@ -326,13 +332,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
       for (int k = 0; k < 2; ++k) {
         mbar_init(&bar[F_P_FULL + k], 1);
         mbar_init(&bar[F_PV_DONE + k], 1);
-        mbar_init(&bar[F_META_READ + k], 8);
+        mbar_init(&bar[F_META_READ + k], 4 * kGroups);
       }
-      mbar_init(&bar[F_O_EMPTY], 8);
-      mbar_init(&bar[F_O_FIXED], 8);
+      mbar_init(&bar[F_O_EMPTY], 4 * kGroups);
+      mbar_init(&bar[F_O_FIXED], 4 * kGroups);
       mbar_init(&bar[F_MMA_DONE_B], 1);
-      mbar_init(&bar[F_P8_READY + 0], 8);
-      mbar_init(&bar[F_P8_READY + 1], 8);
+      mbar_init(&bar[F_P8_READY + 0], 4 * kGroups);
+      mbar_init(&bar[F_P8_READY + 1], 4 * kGroups);
       // the first two P messages may land as soon as the cluster is up
       mbar_arrive_expect_tx(&bar[F_P_FULL + 0], L::kMsgBytes);
       mbar_arrive_expect_tx(&bar[F_P_FULL + 1], L::kMsgBytes);
@@ -379,7 +385,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
   if (rank == 0) {
     uint8_t* sK = smem + L::kKOff;
     uint8_t* sQr = smem + L::kQr8Off;
-    uint8_t* sPs = smem + L::kPsOff;
     if (warp == 0) {
       // ------------------------------------------------ rank 0: TMA producer
       // Converged warp: every lane polls the stage barrier, lane l issues box
@@ -513,7 +518,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
       // barrier 2); both groups (named barrier 1, 256 threads) then share the
       // tiles' softmax by columns.  Every exit decision is made together
       // through named_bar_and.
-      const int grp = warp >= 8 ? 1 : 0;
+      const int grp = (warp - 4) >> 2;
       const int r = (threadIdx.x - 128) & 127;   // TMEM lane == head row
       const int wq = warp & 3;
       const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
@@ -561,39 +566,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
           l = 0.f;
         }
         const int sb = g & 1;
-        if (!named_bar_and(1, 256, qok && wait_lazy(&bar[F_S_FULL + sb], (g >> 1) & 1))) {
+        if (!named_bar_and(1, 128 * kGroups, qok && wait_lazy(&bar[F_S_FULL + sb], (g >> 1) & 1))) {
           ok = false;
           break;
         }
-        if (it.first() && it.newq && grp == 1) fs = s_fs[r];
+        if (kGroups > 1 && it.first() && it.newq && grp == 1) fs = s_fs[r];
         tc_fence_after();
-        // this group's columns [c0, c0 + 64) of the tile: one TMEM read (two
-        // loads, one wait), after which the S buffer goes back to the MMA
-        const int c0 = 64 * grp;
+        // this group's columns [c0, c0 + kSCols) of the tile, read from TMEM
+        // 32 at a time, each folded into the row max before the next is
+        // issued; then the S buffer goes back to the MMA
+        const int c0 = kSCols * grp;
         const int nvalid = min(TILE, ui.hi - (ui.lo + it.j * TILE)) - c0;
         const uint32_t sa = tmem + lane_base + kSCol + sb * TILE + c0;
-        uint32_t v[64];
-        {
-          uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(v);
-          uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 32);
-          tmem_ld32(sa, v0);
-          tmem_ld32(sa + 32, v1);
-          tmem_wait_ld(v0, v1);
+        float v[kSCols];
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < kSCols / 32; ++c) {
+          uint32_t w[32];
+          tmem_ld32(sa + 32 * c, w);
+          tmem_wait_ld(w);
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            v[32 * c + t] = __uint_as_float(w[t]);
+            if (32 * c + t < nvalid) mx[t & 3] = fmaxf(mx[t & 3], v[32 * c + t]);
+          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[F_S_EMPTY + sb]);
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        const float my_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        if (kGroups > 1) s_rowmax[grp][r] = my_max;
+        // rank 1's landing slot sb is free again once the PV MMAs of tile
+        // g - 2 have read it (F_PFREE); the barrier also exchanges the maxima
+        bool sfree = true;
+        if (threadIdx.x == 128 && g >= 2) sfree = wait_cl(&bar[F_PFREE + sb], ((g >> 1) - 1) & 1);
+        if (!named_bar_and(1, 128 * kGroups, sfree)) { ok = false; break; }
+        float row_max = my_max;
+        if (kGroups > 1)
 #pragma unroll
-        for (int t = 0; t < 64; ++t)
-          if (t < nvalid) mx[t & 3] = fmaxf(mx[t & 3], __uint_as_float(v[t]));
-        s_rowmax[grp][r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        // the P message buffer is free once rank 1 reports the previous
-        // message landed (F_MSG_FREE); one barrier also exchanges the maxima
-        bool mfree = true;
-        if (threadIdx.x == 128 && g >= 1) mfree = wait_cl(&bar[F_MSG_FREE], (g - 1) & 1);
-        if (!named_bar_and(1, 256, mfree)) { ok = false; break; }
-        const float mt = fmaxf(s_rowmax[0][r], s_rowmax[1][r]) * fs;   // fs > 0
+          for (int k = 0; k < kGroups; ++k) row_max = fmaxf(row_max, s_rowmax[k][r]);
+        const float mt = row_max * fs;   // fs > 0
 
         // ---- online softmax in the log2 domain
         bool need_rescale = false;
@@ -606,52 +618,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
           m = mt;
         }
 
-        // ---- P message for rank 1: p' = 2^6 exp2(s - m) in fp16, this
-        // group's 64 tokens = its 16 KB tile of the message
-        uint8_t* msg = sPs + grp * 16384;
+        // ---- P message, written into rank 1's slot sb with st.async (each
+        // store completes its bytes on rank 1's F_P_FULL[sb]): p' = 2^6
+        // exp2(s - m) in fp16, this group's 64 tokens = its 16 KB tile
+        const uint32_t rmsg = precv_peer + sb * L::kMsgStride;
+        const uint32_t rbar = pfull_peer + sb * 8;
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
         const float mp = static_cast<float>(kPShift) - m;
+        // all of p first (independent exp2s), then the packed stores
 #pragma unroll
-        for (int uu = 0; uu < 8; ++uu) {
-          float p[8];
+        for (int t = 0; t < kSCols; ++t) {
+          // masked columns: 0; others p' <= 2^8
+          v[t] = t < nvalid ? fast_exp2(fmaf(v[t], fs, mp)) : 0.f;
+          ps[t & 3] += v[t];
+        }
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int t = 8 * uu + e;
-            // masked columns: 0; others p' <= 2^8
-            p[e] = t < nvalid ? fast_exp2(fmaf(__uint_as_float(v[t]), fs, mp)) : 0.f;
-            ps[e & 3] += p[e];
-          }
-          *reinterpret_cast<uint4*>(msg + sw128_offset(r, uu)) =
-              make_uint4(pack2<false>(p[0], p[1]), pack2<false>(p[2], p[3]),
-                         pack2<false>(p[4], p[5]), pack2<false>(p[6], p[7]));
+        for (int uu = 0; uu < kSCols / 8; ++uu) {
+          const float* p = v + 8 * uu;
+          // 64 tokens per 16 KB tile of the message, 8 per 16-byte unit
+          const int tok = c0 + 8 * uu;
+          st_async_v4(rmsg + (tok >> 6) * 16384 + sw128_offset(r, (tok & 63) >> 3),
+                      make_uint4(pack2<false>(p[0], p[1]), pack2<false>(p[2], p[3]),
+                                 pack2<false>(p[4], p[5]), pack2<false>(p[6], p[7])),
+                      rbar);
         }
         l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));   // this group's half of the row sum of p'
-        msg = sPs;
         if (grp == 0) {
-          reinterpret_cast<float*>(msg + L::kMsgAlpha)[r] = alpha;
-          reinterpret_cast<float*>(msg + L::kMsgLA)[r] = l;
-          reinterpret_cast<float*>(msg + L::kMsgM)[r] = m;
+          st_async_b32(rmsg + L::kMsgAlpha + 4 * r, __float_as_uint(alpha), rbar);
+          st_async_b32(rmsg + L::kMsgLA + 4 * r, __float_as_uint(l), rbar);
+          st_async_b32(rmsg + L::kMsgM + 4 * r, __float_as_uint(m), rbar);
           // (both groups take the same rescale decisions: group A's flags)
           const uint32_t any = __any_sync(0xffffffffu, need_rescale) ? 1u : 0u;
           if (lane == 0) warp_flags[wq] = any;
+          if (kGroups == 1) st_async_b32(rmsg + L::kMsgLB + 4 * r, 0u, rbar);
         } else {
-          reinterpret_cast<float*>(msg + L::kMsgLB)[r] = l;
+          st_async_b32(rmsg + L::kMsgLB + 4 * r, __float_as_uint(l), rbar);
         }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 256);
+        named_bar_sync(1, 128 * kGroups);   // every store of the message is issued
         if (threadIdx.x == 128) {
           const uint32_t flags = (warp_flags[0] | warp_flags[1] | warp_flags[2] | warp_flags[3]) |
                                  (it.last() ? 2u : 0u);
-          *reinterpret_cast<volatile uint32_t*>(msg + L::kMsgHdr) = flags;
-          fence_proxy_async_smem();
-          if (g >= 2 && !wait_cl(&bar[F_PFREE + sb], ((g >> 1) - 1) & 1)) ok = false;
-          if (ok) {
-            bulk_copy_to_peer(precv_peer + sb * L::kMsgStride, msg, L::kMsgBytes,
-                              pfull_peer + sb * 8);
-            *msg_count = g + 1;
-          }
+          st_async_v4(rmsg + L::kMsgHdr, make_uint4(flags, 0u, 0u, 0u), rbar);
+          *msg_count = g + 1;   // messages sent (for rank 1's drain)
         }
-        ok = named_bar_and(1, 256, ok && !*abort_flag);
+        ok = named_bar_and(1, 128 * kGroups, ok && !*abort_flag);
         it.advance(pp);
         ++g;
         cq += 1;
@@ -791,29 +801,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
           }
         }
       }
-      // ------------------------------------------------ rank 1: P landing watcher
-      // Reports each P message to rank 0 once it has landed (the sender's
-      // single buffer is then free) and counts them for the final drain.
-      if (lane == 0) {
-        const uint32_t msgfree_peer = map_to_peer(&bar[F_MSG_FREE], 0);
-        TileIter<TILE> it;
-        it.start(pp, rng);
-        int g = 0;
-        while (it.valid) {
-          if (!wait(&bar[F_P_FULL + (g & 1)], (g >> 1) & 1)) break;
-          *msg_count = g + 1;
-          mbar_arrive_remote(msgfree_peer);
-          it.advance(pp);
-          ++g;
-        }
-      }
     } else {
       // ------------------------------------------------ rank 1: O rescale + epilogue
-      // group A: latent columns [0, 256), group B: [256, 512) of row r
-      const int grp = warp >= 8 ? 1 : 0;
+      // group k: latent columns [k kOCols, (k + 1) kOCols) of row r
+      const int grp = (warp - 4) >> 2;
       const int r = (threadIdx.x - 128) & 127;
       const int wq = warp & 3;
-      const int cbeg = 256 * grp;
+      const int cbeg = kOCols * grp;
       const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
       TileIter<TILE> it;
       it.start(pp, rng);
@@ -823,16 +817,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
         const UnitInfo ui = it.ui;
         const int sb = g & 1;
         if (!wait_lazy(&bar[F_P_FULL + sb], (g >> 1) & 1)) { ok = false; break; }
+        if (threadIdx.x == 128) *msg_count = g + 1;   // messages seen to land (for the drain)
         uint8_t* msg = sPr + sb * L::kMsgStride;
         const uint32_t hdr = *reinterpret_cast<const volatile uint32_t*>(msg + L::kMsgHdr);
         const float alpha = reinterpret_cast<const float*>(msg + L::kMsgAlpha)[r];
         const float lsum = reinterpret_cast<const float*>(msg + L::kMsgLA)[r] +
                            reinterpret_cast<const float*>(msg + L::kMsgLB)[r];
         const float m2 = reinterpret_cast<const float*>(msg + L::kMsgM)[r];
-        {
-          // row r of this group's 64 tokens: fp16 p' -> [hi bytes | lo bytes]
+#pragma unroll 1
+        for (int tile = grp * (2 / kGroups); tile < (grp + 1) * (2 / kGroups); ++tile) {
+          // row r of 64-token tile `tile`: fp16 p' -> [hi bytes | lo bytes]
           // in the same 128-byte row (each thread rewrites only its own row)
-          uint8_t* row = msg + grp * 16384;
+          uint8_t* row = msg + tile * 16384;
           uint4 x[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) x[u] = *reinterpret_cast<const uint4*>(row + sw128_offset(r, u));
@@ -855,10 +851,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
             *reinterpret_cast<uint4*>(row + sw128_offset(r, 4 + u)) =
                 make_uint4(lw[4 * u], lw[4 * u + 1], lw[4 * u + 2], lw[4 * u + 3]);
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar[F_P8_READY + sb]);
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[F_P8_READY + sb]);
         // the message's header fields are in registers: the slot may go back
         // (once the PV MMAs have read its P as well)
         __syncwarp();
@@ -867,7 +863,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
           // O *= alpha before PV of this tile; PV of the previous tile must be done
           if (!wait_lazy(&bar[F_PV_DONE + ((g - 1) & 1)], ((g - 1) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          rescale_o(tmem + lane_base, cbeg, alpha);
+          rescale_o<kOCols>(tmem + lane_base, cbeg, alpha);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bar[F_O_FIXED]);
@@ -886,10 +882,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
           const bool whole = it.whole();
           const int slot = 2 * cid + (it.u == rng.u_begin ? 0 : 1);
           if (whole)
-            store_o_half(tmem + lane_base, cbeg, pp.o_part, row_out * 512, mul, pp.part_dtype,
+            store_o_half<kOCols>(tmem + lane_base, cbeg, pp.o_part, row_out * 512, mul, pp.part_dtype,
                          r < pp.H);
           else
-            store_o_half(tmem + lane_base, cbeg, pp.ws_o, (static_cast<int64_t>(slot) * 128 + r) * 512,
+            store_o_half<kOCols>(tmem + lane_base, cbeg, pp.ws_o, (static_cast<int64_t>(slot) * 128 + r) * 512,
                          mul, pp.part_dtype, true);
           tc_fence_before();
           __syncwarp();
@@ -914,9 +910,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8Threads, 1)
   if (pp.split && rank == 1 && threadIdx.x == 0) record_split_unit<TILE>(pp, cid, rng, shares, split);
   cluster_sync();
   if (rank == 1 && threadIdx.x == 64) {
-    // Drain the P messages rank 0 sent that the watcher never saw land (it
-    // stops early when a wait runs out): rank 0 must not exit while its
-    // copies still read its buffer, nor rank 1 while they still write here.
+    // Drain the P messages rank 0 sent that the epilogue warps never saw
+    // land (they stop early when a wait runs out): rank 1 must not exit while
+    // rank 0's stores still write here.  Every message went to an armed slot,
+    // so each complete one completes a P_FULL phase.
     const uint32_t sent_addr = map_to_peer(const_cast<int*>(msg_count), 0);
     int sent;
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(sent) : "r"(sent_addr) : "memory");

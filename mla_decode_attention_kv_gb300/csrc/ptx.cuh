@@ -217,6 +217,23 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const vo
       : "memory");
 }
 
+// Asynchronous stores into a peer CTA's shared memory (shared::cluster
+// addresses from mapa): each completes its bytes as transaction count on the
+// peer's mbarrier (also a shared::cluster address), so a consumer that waits
+// on that barrier sees the data, as with a TMA load.
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, uint4 v, uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(raddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_async_b32(uint32_t raddr, uint32_t v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(raddr),
+               "r"(v), "r"(rbar)
+               : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
