@@ -77,14 +77,15 @@ def exchange_partials(o_send: torch.Tensor, lse_send: torch.Tensor, group=None):
 
 def dcp_decode_step(q_abs, q_pe, kv_cache, block_table, seq_lens, W_UV, num_shards: int, *,
                     kv_cur=None, group=None, scale: float = api.DEFAULT_SCALE, part_dtype=None,
-                    err_flag=None, stream=None, workspace="default"):
+                    err_flag=None, stream=None, workspace="default", kv_scale=None):
     """One decode step of MLA with the history split over the ranks of ``group``.
 
     Every rank passes the same q_abs [B, q, H, 512], q_pe, kv_cur and W_UV,
     and its own piece of the history: kv_cache, block_table and seq_lens of
     that piece (``local_block_table`` builds them from a whole table), split
     into ``num_shards`` shards on this GPU.  H must be a multiple of the group
-    size N.  Returns this rank's heads [r*H/N, (r+1)*H/N): the output
+    size N.  An E4M3 cache (uint8 / float8_e4m3fn bytes, with ``kv_scale``)
+    takes the FP8 partial kernel, as in ``api.mla_dcp_decode_partial``.  Returns this rank's heads [r*H/N, (r+1)*H/N): the output
     [B*q, (H/N)*128], the combined latent [B*q, H/N, 512] and its LSE
     [B*q, H/N]."""
     world = dist.get_world_size(group)
@@ -96,7 +97,7 @@ def dcp_decode_step(q_abs, q_pe, kv_cache, block_table, seq_lens, W_UV, num_shar
     o_send, lse_send = api.mla_dcp_decode_partial(
         q_abs, q_pe, kv_cache, block_table, seq_lens, num_shards, kv_cur=kv_cur, scale=scale,
         part_dtype=part_dtype, err_flag=err_flag, stream=stream, workspace=workspace,
-        head_slices=world)
+        head_slices=world, kv_scale=kv_scale)
     if world == 1:
         o_send = o_send.view(1, -1, *o_send.shape[2:])
         lse_send = lse_send.view(1, -1, *lse_send.shape[2:])
