@@ -49,7 +49,8 @@ namespace mla {
 
 // Shared-memory plan (offsets from a 1024-aligned base; same size on both
 // ranks).  Rank 0: K ring, Q RoPE tile, one outgoing P message.
-// Rank 1: V ring, two incoming P messages.  Barriers at one common offset.
+// Rank 1: V ring, two incoming P messages, the epilogue's staging rows.
+// Barriers at one common offset.
 //
 // A ring stage is one mbarrier phase.  Each phase costs an SM a fixed few
 // hundred nanoseconds however many bytes it carries (measured on GB300: a
@@ -84,7 +85,8 @@ struct PairSmem {
   // rank 1
   static constexpr int kVOff = 0;
   static constexpr int kPrOff = kVOff + kNV * kVStage;       // 131072
-  static constexpr int kEnd1 = kPrOff + 2 * kMsgStride;      // 200704
+  static constexpr int kStgOff = kPrOff + 2 * kMsgStride;    // 200704: 4 KB per epilogue warp
+  static constexpr int kEnd1 = kStgOff + 4 * 4096;           // 217088
   static constexpr int kBarOff = kEnd0 > kEnd1 ? kEnd0 : kEnd1;
   static constexpr int kTotal = kBarOff + 512 + 1024;
 };
@@ -117,6 +119,61 @@ enum : int {
 // barriers + TMEM slot + abort flag + 4 warp flags + Q-stage counters + the
 // P message count must fit the barrier block
 static_assert((B_COUNT + 9) * 8 <= 512, "barrier block");
+
+// Epilogue of one piece, rows of this warp: row r (TMEM lane r) of O times
+// `mul`, in the partial dtype, to `dst_row` (this thread's output row, or
+// nullptr for a row that is not stored).  Per 128-byte column chunk, each
+// lane writes its row into the warp's 4 KB of staging (16-byte unit j of row
+// r at unit j ^ (r & 7), so neither the row writes nor the read-back below
+// conflict on banks), then the warp stores the chunk back four rows per
+// instruction: each store covers whole 128-byte row segments instead of one
+// 32-byte piece of 32 different rows.  The warp's O_EMPTY arrival comes after
+// its last store is issued: released as soon as the last TMEM load had landed,
+// the next unit's PV MMAs ran against the staging traffic and the very long
+// context was 1 % slower.
+__device__ __forceinline__ void epilogue_rows(uint32_t ta, uint32_t stg, char* dst_row, float mul,
+                                              int dt, int lane, uint64_t* o_empty) {
+  const bool f32 = dt == kFP32;
+  const int nchunk = f32 ? 16 : 8;
+  for (int c = 0; c < nchunk; ++c) {
+    uint32_t w[32];
+    if (f32) {
+      uint32_t v[32];
+      tmem_ld32(ta + c * 32, v);
+      tmem_wait_ld(v);
+#pragma unroll
+      for (int t = 0; t < 32; ++t) w[t] = __float_as_uint(__uint_as_float(v[t]) * mul);
+    } else {
+      uint32_t v0[32], v1[32];
+      tmem_ld32(ta + c * 64, v0);
+      tmem_ld32(ta + c * 64 + 32, v1);
+      tmem_wait_ld(v0, v1);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        w[k] = pack2_dt(__uint_as_float(v0[2 * k]) * mul, __uint_as_float(v0[2 * k + 1]) * mul, dt);
+        w[16 + k] =
+            pack2_dt(__uint_as_float(v1[2 * k]) * mul, __uint_as_float(v1[2 * k + 1]) * mul, dt);
+      }
+    }
+    __syncwarp();   // the read-back of the previous chunk is done
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_v4(stg + lane * 128 + ((j ^ (lane & 7)) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2],
+                   w[4 * j + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int rr = it * 4 + (lane >> 3), j = lane & 7;
+      char* d = reinterpret_cast<char*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dst_row), rr));
+      const uint4 x = ld_shared_v4(stg + rr * 128 + ((j ^ (rr & 7)) << 4));
+      if (d != nullptr) *reinterpret_cast<uint4*>(d + c * 128 + j * 16) = x;
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(o_empty);
+}
 
 template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
@@ -688,6 +745,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       const int r = threadIdx.x - 128;
       const int wq = warp & 3;
       const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+      const uint32_t stg = smem_u32(smem + L::kStgOff + wq * 4096);
       TileIter<TILE> it;
       it.start(pp, rng);
       int g = 0;
@@ -730,41 +788,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           const int64_t row_out =
               part_row(pp, static_cast<int64_t>(ui.b) * pp.q_len + ui.i, ui.p, r);   // r < H only
           const float inv_l = 1.f / lsum;
-          if (it.whole()) {
-            // two TMEM loads in flight per wait
-            for (int c0 = 0; c0 < 512; c0 += 64) {
-              uint32_t v0[32], v1[32];
-              tmem_ld32(tmem + lane_base + c0, v0);
-              tmem_ld32(tmem + lane_base + c0 + 32, v1);
-              tmem_wait_ld(v0, v1);
-              if (r < pp.H) {
-                store_row32(pp.o_part, row_out * 512 + c0, v0, inv_l, pp.part_dtype);
-                store_row32(pp.o_part, row_out * 512 + c0 + 32, v1, inv_l, pp.part_dtype);
-              }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[B_O_EMPTY]);
-            if (r < pp.H) pp.lse_part[row_out] = lse2 * kLn2;
-          } else {
-            // a piece of a unit split across pairs: park O / l (in the
-            // partial dtype) and the LSE in this pair's workspace slot; the
-            // pieces are merged after the main loop
-            const int slot = 2 * cid + (it.u == rng.u_begin ? 0 : 1);
-            for (int c0 = 0; c0 < 512; c0 += 64) {
-              uint32_t v0[32], v1[32];
-              tmem_ld32(tmem + lane_base + c0, v0);
-              tmem_ld32(tmem + lane_base + c0 + 32, v1);
-              tmem_wait_ld(v0, v1);
-              const int64_t e = (static_cast<int64_t>(slot) * 128 + r) * 512 + c0;
-              store_row32(pp.ws_o, e, v0, inv_l, pp.part_dtype);
-              store_row32(pp.ws_o, e + 32, v1, inv_l, pp.part_dtype);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[B_O_EMPTY]);
+          const int64_t row_bytes = pp.part_dtype == kFP32 ? 2048 : 1024;
+          // A piece of a unit split across pairs parks O / l (in the partial
+          // dtype) and the LSE in this pair's workspace slot instead; the
+          // pieces are merged after the main loop (rows < H only).
+          const bool whole = it.whole();
+          const int slot = 2 * cid + (it.u == rng.u_begin ? 0 : 1);
+          char* dst = nullptr;
+          if (r < pp.H)
+            dst = whole ? static_cast<char*>(pp.o_part) + row_out * row_bytes
+                        : static_cast<char*>(pp.ws_o) + (static_cast<int64_t>(slot) * 128 + r) * row_bytes;
+          epilogue_rows(tmem + lane_base, stg, dst, inv_l, pp.part_dtype, lane, &bar[B_O_EMPTY]);
+          if (!whole)
             pp.ws_lse[slot * 128 + r] = lse2;
-          }
+          else if (r < pp.H)
+            pp.lse_part[row_out] = lse2 * kLn2;
         }
         it.advance(pp);
         ++g;

@@ -53,6 +53,23 @@ __device__ __noinline__ UnitInfo unit_info(const PartialParams& pp, int u) {
   return ui;
 }
 
+// The first units of a pair's range, looked up once when the kernel starts
+// (partition_tiles fills the table): every role's tile iterator then reads a
+// unit's geometry from shared memory instead of recomputing it, with a
+// seq_lens load and integer divisions, on its issue path at each unit
+// boundary.  Units past the table are computed as before.
+constexpr int kUnitCache = 64;
+__shared__ UnitInfo s_unit_cache[kUnitCache];
+__shared__ int s_unit_range[2];   // first unit of the table, entries
+
+// (out of line, like unit_info: the iterators' copies stay off the hot loops)
+template <int TILE>
+__device__ __noinline__ UnitInfo unit_get(const PartialParams& pp, int u) {
+  const unsigned k = static_cast<unsigned>(u - s_unit_range[0]);
+  if (k < static_cast<unsigned>(s_unit_range[1])) return s_unit_cache[k];
+  return unit_info<TILE>(pp, u);
+}
+
 // Row of o_part / lse_part holding token t (= b * q_len + i), part p, head h.
 // The partials are laid out as head_slices blocks of H / head_slices heads,
 // [head_slices][T][P][H / head_slices]; with one slice that is [T][P][H].
@@ -91,7 +108,7 @@ struct TileIter {
     valid = r.u_begin <= r.u_last;
     if (!valid) return;
     u = r.u_begin;
-    ui = unit_info<TILE>(pp, u);
+    ui = unit_get<TILE>(pp, u);
     ustart = r.t_begin - r.j_begin;
     enter(pp, r.j_begin);
   }
@@ -110,7 +127,7 @@ struct TileIter {
     while (u < u_last) {
       ustart += ui.ntiles;
       ++u;
-      ui = unit_info<TILE>(pp, u);
+      ui = unit_get<TILE>(pp, u);
       if (ui.ntiles > 0) {
         enter(pp, 0);
         return;
@@ -247,6 +264,15 @@ __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid
   rng.u_last = s_rng[2];
   rng.j_stop = split ? s_rng[3] : (rng.u_last >= 0 ? unit_info<TILE>(pp, rng.u_last).ntiles : 0);
   rng.t_begin = static_cast<int>(lo);
+  // the unit table of this range (every thread of the CTA passes here)
+  const int ncache = rng.u_begin <= rng.u_last ? min(rng.u_last - rng.u_begin + 1, kUnitCache) : 0;
+  if (static_cast<int>(threadIdx.x) < ncache)
+    s_unit_cache[threadIdx.x] = unit_info<TILE>(pp, rng.u_begin + static_cast<int>(threadIdx.x));
+  if (threadIdx.x == 0) {
+    s_unit_range[0] = rng.u_begin;
+    s_unit_range[1] = ncache;
+  }
+  __syncthreads();
 }
 
 // Record, for the merge kernel, the split unit whose last tile pair `cid`
