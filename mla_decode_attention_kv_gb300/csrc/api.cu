@@ -241,15 +241,17 @@ int decode_partial(bool kv8, const void* q_abs, const void* q_pe, const void* kv
   pp.ws_o = nullptr;
   pp.ws_lse = nullptr;
   pp.ws_units = nullptr;
+  pp.ws_bounds = nullptr;
   if (workspace) {
     const int clusters = mla::partial_max_clusters();
     if (clusters < 1) return MLA_ERR_CUDA;
     const int part_bytes = part_dtype == MLA_FP32 ? 4 : 2;
     if (workspace_bytes < mla::partial_workspace_bytes(clusters, part_bytes)) return MLA_ERR_BAD_SHAPE;
-    const size_t recs = (static_cast<size_t>(clusters + 1) * 16 + 255) / 256 * 256;
+    const size_t recs = mla::partial_workspace_recs(clusters);
     char* w = static_cast<char*>(workspace);
     pp.split = clusters;
     pp.ws_units = reinterpret_cast<int4*>(w);
+    pp.ws_bounds = reinterpret_cast<int*>(w + static_cast<size_t>(clusters + 1) * 16);
     pp.ws_lse = reinterpret_cast<float*>(w + recs);
     pp.ws_o = w + recs + 2 * static_cast<size_t>(clusters) * 128 * 4;
   }

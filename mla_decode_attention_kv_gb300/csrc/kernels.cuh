@@ -26,18 +26,26 @@ struct PartialParams {
   // Split-unit workspace (split = number of CTA pairs, 0 = whole units):
   // per pair two slots of O / l and LSE (log2, [128]) for the units cut at
   // the ends of its share, and per pair the record of the split unit whose
-  // last tile it holds (+ one header record), read by the merge kernel.
+  // last tile it holds (+ one header record) and the table of the pairs'
+  // share boundaries, read by the merge kernel.
   int split;
   void* ws_o;            // pieces of O / l in the partial dtype, [2*pairs][128][512]
   float* ws_lse;         // [2*pairs][128]
   int4* ws_units;        // [pairs + 1]: {unit, first tile, first pair, last pair}; header {T, pairs}
+  int* ws_bounds;        // [pairs + 1]: first tile of each pair's share, then the tile total
 };
+
+// Bytes of the workspace's record block: the unit records and the share
+// boundaries, rounded up to 256.
+inline size_t partial_workspace_recs(int clusters) {
+  return (static_cast<size_t>(clusters + 1) * (16 + 4) + 255) / 256 * 256;
+}
 
 // Workspace of the partial kernel for `clusters` CTA pairs and partials of
 // `part_bytes` bytes per element (4 covers every partial dtype).
 inline size_t partial_workspace_bytes(int clusters, int part_bytes = 4) {
   const size_t slots = 2 * static_cast<size_t>(clusters);
-  const size_t recs = (static_cast<size_t>(clusters + 1) * 16 + 255) / 256 * 256;
+  const size_t recs = partial_workspace_recs(clusters);
   return recs + slots * 128 * 4 + slots * 512 * 128 * static_cast<size_t>(part_bytes);
 }
 int partial_max_clusters();

@@ -847,7 +847,7 @@ __global__ void __launch_bounds__(256) mla_partial_merge_kernel(PartialParams pp
   const int u = rec.x;
   if (u < 0) return;
   const int4 hdr = pp.ws_units[gridDim.x];
-  const Shares sh{hdr.x, hdr.y};
+  const Shares sh{pp.ws_bounds, hdr.x, hdr.y};
   const int64_t ustart = rec.y;
   const int c_first = rec.z, c_last = rec.w;
   auto share_start = [&](int c) { return sh.start(c); };

@@ -152,26 +152,43 @@ struct TileIter {
 };
 
 // Tile shares of the CTA pairs: pair c takes tiles [start(c), start(c + 1))
-// of the flat order of all units' tiles.
+// of the flat order of all units' tiles.  The boundaries are a table made by
+// partition_tiles (equal shares of cost, below), kept in shared memory by the
+// partial kernels and in the workspace for the merge kernel.
 struct Shares {
-  int64_t total;
+  const int* bound;   // [ncl + 1], non-decreasing, bound[0] = 0, bound[ncl] = total
+  int64_t total;      // tiles of all units
   int ncl;
-  __device__ __forceinline__ int64_t start(int c) const {
-    return static_cast<int64_t>(c) * total / ncl;
-  }
+  __device__ __forceinline__ int64_t start(int c) const { return bound[c]; }
   __device__ __forceinline__ int cluster_of(int64_t t) const {   // the pair whose share holds tile t
-    int c = static_cast<int>(t * ncl / total);
-    while (c + 1 < ncl && start(c + 1) <= t) ++c;
-    while (c > 0 && start(c) > t) --c;
-    return c;
+    int lo = 0, hi = ncl - 1;   // the last c with start(c) <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (bound[mid] <= t)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    return lo;
   }
 };
 
+// Cost of a unit for the shares, in half tiles: its tiles, plus half a tile
+// for what every piece costs a pair besides its tiles (the restart of the
+// pipelines at a new unit, the epilogue).  Measured on GB300 with a batch of
+// ragged histories (64 sequences of 512 to 65536 tokens in 16 shards): with
+// equal tile shares a pair's finishing time grew by ~1.7 us, about half a
+// tile, per piece it held, and the pairs held 3 to 56 pieces.
+constexpr int kCostPerTile = 2;
+constexpr int kCostPerUnit = 1;
+
 // Tile share of pair `cid`: tiles [lo, hi) of the flat order of all units'
-// tiles, lo = cid * T / ncl.  With a workspace the share is exact and the
-// units at its ends may be split with the neighbouring pairs (their pieces
-// are merged through the workspace); without one the pair owns the whole
-// units whose first tile falls in its share.  Units without tiles (o = 0,
+// tiles, where the boundaries split the units' total cost (kCostPerTile per
+// tile plus kCostPerUnit per unit with tiles) into equal parts: a tile belongs
+// to the pair whose part holds the tile's start.  With a workspace the share
+// is exact and the units at its ends may be split with the neighbouring pairs
+// (their pieces are merged through the workspace); without one the pair owns
+// the whole units whose first tile falls in its share.  Units without tiles (o = 0,
 // lse = -inf) are dealt round-robin elsewhere: unit u to pair u mod pairs.
 // Both CTAs of a pair compute the same range.  Called by all NT threads of
 // the CTA (a multiple of 32, at most 512; at most 256 pairs).
@@ -180,9 +197,10 @@ __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid
                                                 TileRange& rng, Shares& sh, bool& split) {
   static_assert(NT % 32 == 0 && NT <= 512, "block size");
   constexpr int kWarps = NT / 32;
-  __shared__ int s_scan[kWarps];
+  __shared__ unsigned long long s_scan[kWarps];
   __shared__ int s_load[256];
   __shared__ int s_rng[4];
+  __shared__ int s_bound[257];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   sh.total = 0;
@@ -192,13 +210,19 @@ __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid
   const int per = (U + NT - 1) / NT;
   const int a = min(U, static_cast<int>(threadIdx.x) * per);
   const int e = min(U, a + per);
-  int cnt = 0;
-  for (int u = a; u < e; ++u) cnt += unit_info<TILE>(pp, u).ntiles;
-  // exclusive block scan of cnt: warp inclusive scans, then the warp totals
-  int incl = cnt;
+  int cnt = 0, cost = 0;   // tiles and cost of this thread's units
+  for (int u = a; u < e; ++u) {
+    const int nt = unit_info<TILE>(pp, u).ntiles;
+    cnt += nt;
+    cost += nt > 0 ? kCostPerTile * nt + kCostPerUnit : 0;
+  }
+  // exclusive block scan of (cost, tiles), packed in one 64-bit word (both
+  // sums stay below 2^32): warp inclusive scans, then the warp totals
+  const unsigned long long mine = (static_cast<unsigned long long>(cost) << 32) | static_cast<unsigned>(cnt);
+  unsigned long long incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
   if (lane == 31) s_scan[warp] = incl;
@@ -210,31 +234,64 @@ __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid
   }
   for (int c = threadIdx.x; c < ncl; c += NT) s_load[c] = 0;
   __syncthreads();
-  int warp_base = 0, all = 0;
+  unsigned long long warp_base = 0, all = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) {
-    const int t = s_scan[w];
+    const unsigned long long t = s_scan[w];
     warp_base += w < warp ? t : 0;
     all += t;
   }
-  const int my_start = warp_base + incl - cnt;   // tiles before this thread's units
-  sh.total = all;
+  const unsigned long long before = warp_base + incl - mine;
+  const int my_start = static_cast<int>(before & 0xffffffffu);      // tiles before this thread's units
+  const int64_t my_cstart = static_cast<int64_t>(before >> 32);     // their cost
+  const int64_t all_cost = static_cast<int64_t>(all >> 32);
+  sh.total = static_cast<int64_t>(all & 0xffffffffu);
+  sh.ncl = ncl;
+  sh.bound = s_bound;
+  // Share boundaries: bound[c] = the tiles whose start lies below the cost
+  // target floor(c * cost / ncl).  Every target falls in exactly one unit with
+  // tiles (their cost ranges tile [0, cost)), whose thread writes it.
+  if (all_cost > 0) {
+    int64_t trun = my_start, crun = my_cstart;
+    for (int u = a; u < e; ++u) {
+      const int nt = unit_info<TILE>(pp, u).ntiles;
+      if (nt == 0) continue;
+      const int64_t cend = crun + kCostPerTile * nt + kCostPerUnit;
+      for (int c = max(1, static_cast<int>((crun * ncl + all_cost - 1) / all_cost)); c < ncl; ++c) {
+        const int64_t tc = static_cast<int64_t>(c) * all_cost / ncl;
+        if (tc >= cend) break;
+        // tile j of the unit starts at crun + kCostPerUnit + kCostPerTile * j
+        const int64_t into = tc - crun - kCostPerUnit;
+        const int64_t j = into <= 0 ? 0 : min(static_cast<int64_t>(nt), (into + kCostPerTile - 1) / kCostPerTile);
+        s_bound[c] = static_cast<int>(trun + j);
+      }
+      trun += nt;
+      crun = cend;
+    }
+  } else {
+    for (int c = threadIdx.x; c <= ncl; c += NT) s_bound[c] = 0;
+  }
+  if (threadIdx.x == 0) {
+    s_bound[0] = 0;
+    s_bound[ncl] = static_cast<int>(sh.total);
+  }
+  __syncthreads();
   if (pp.split && sh.total > 0) {
     // Split units only where whole units would leave the busiest pair above
-    // the even share by more than max(2 tiles, 1/8 of the share): the merge
-    // kernel and the extra unit ends cost about that much.
+    // the even share of cost by more than max(3 tiles, 1/8 of the share): the
+    // merge kernel and the extra unit ends cost about that much.
     int64_t run = my_start;
     for (int u = a; u < e; ++u) {
       const int nt = unit_info<TILE>(pp, u).ntiles;
-      if (nt > 0) atomicAdd(&s_load[sh.cluster_of(run)], nt);
+      if (nt > 0) atomicAdd(&s_load[sh.cluster_of(run)], kCostPerTile * nt + kCostPerUnit);
       run += nt;
     }
     __syncthreads();
     int mx = 0;
     for (int c = threadIdx.x; c < ncl; c += NT) mx = max(mx, s_load[c]);
-    const int64_t even = (sh.total + ncl - 1) / ncl;
+    const int64_t even = (all_cost + ncl - 1) / ncl;
     // any pair above the threshold decides for all
-    split = __syncthreads_or(mx > even + max(int64_t{2}, even / 8)) != 0;
+    split = __syncthreads_or(mx > even + max(int64_t{3 * kCostPerTile}, even / 8)) != 0;
   }
   const int64_t lo = sh.start(cid);
   const int64_t hi = sh.start(cid + 1);
@@ -291,7 +348,11 @@ __device__ __forceinline__ void record_split_unit(const PartialParams& pp, int c
     }
   }
   pp.ws_units[cid] = rec;
-  if (cid == 0) pp.ws_units[sh.ncl] = make_int4(static_cast<int>(sh.total), sh.ncl, 0, 0);
+  pp.ws_bounds[cid] = static_cast<int>(sh.start(cid));
+  if (cid == 0) {
+    pp.ws_units[sh.ncl] = make_int4(static_cast<int>(sh.total), sh.ncl, 0, 0);
+    pp.ws_bounds[sh.ncl] = static_cast<int>(sh.total);
+  }
 }
 
 // Protocol waits of the pipelines: each gives up after `limit` polls, records
