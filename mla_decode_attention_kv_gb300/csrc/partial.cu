@@ -837,101 +837,82 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 }
 
 // ---------------------------------------------------------------- merge of split units
-// One CTA per (pair, 64-row half): merges the pieces of the split unit whose
-// last tile that pair held (pp.ws_units[pair]) by their LSEs, exactly as the
-// combine merges shards, and writes the unit's o_part rows and lse_part.
+// One CTA per (pair, 32-row quarter): merges the pieces of the split unit
+// whose last tile that pair held (pp.ws_units[pair]) by their LSEs, exactly as
+// the combine merges shards, and writes the unit's o_part rows and lse_part.
+// Eight threads per row, 64 columns each; every thread folds the pieces in
+// pair order into a running (max, weight sum, accumulator) of its own, so the
+// CTA needs no shared memory and no barrier, and a launch takes few dependent
+// memory round trips (record, share boundaries, then each piece's LSE and
+// values together).
 __global__ void __launch_bounds__(256) mla_partial_merge_kernel(PartialParams pp) {
   griddep_wait();   // the partial grid has completed and its writes are visible
   griddep_launch_dependents();
   const int4 rec = pp.ws_units[blockIdx.x];
   const int u = rec.x;
-  if (u < 0) return;
-  const int4 hdr = pp.ws_units[gridDim.x];
-  const Shares sh{pp.ws_bounds, hdr.x, hdr.y};
+  const int r = blockIdx.y * 32 + (threadIdx.x >> 3);
+  if (u < 0 || r >= pp.H) return;
   const int64_t ustart = rec.y;
   const int c_first = rec.z, c_last = rec.w;
-  auto share_start = [&](int c) { return sh.start(c); };
-  __shared__ int s_slot[256];
-  __shared__ float s_w[256 * 32];       // per candidate pair, per row of the pass: weight
-  __shared__ float s_lsetot[32];
-  const int ncand = c_last - c_first + 1;
-  for (int i = threadIdx.x; i < ncand; i += 256) {
-    const int c = c_first + i;
-    s_slot[i] = share_start(c + 1) > share_start(c) ? 2 * c + (share_start(c) >= ustart ? 0 : 1) : -1;
-  }
-  const int sub = threadIdx.x & 7;      // 64-column slice of a row
+  const int sub = threadIdx.x & 7;      // 64-column slice of the row
   const bool f32 = pp.part_dtype == kFP32;
-  for (int pass = 0; pass < 2; ++pass) {
-    const int rbase = blockIdx.y * 64 + pass * 32;
-    __syncthreads();
-    for (int x = threadIdx.x; x < ncand * 32; x += 256) {
-      const int i = x >> 5, rr = x & 31;
-      const int sl = s_slot[i];
-      s_w[x] = (sl >= 0 && rbase + rr < pp.H) ? pp.ws_lse[sl * 128 + rbase + rr] : -INFINITY;
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      const int rr = threadIdx.x;
-      float mx = -INFINITY;
-      for (int i = 0; i < ncand; ++i) mx = fmaxf(mx, s_w[i * 32 + rr]);
-      float wsum = 0.f;
-      for (int i = 0; i < ncand; ++i) wsum += s_slot[i] >= 0 ? exp2f(s_w[i * 32 + rr] - mx) : 0.f;
-      const float inv_w = 1.f / wsum;
-      for (int i = 0; i < ncand; ++i)
-        s_w[i * 32 + rr] = s_slot[i] >= 0 ? exp2f(s_w[i * 32 + rr] - mx) * inv_w : 0.f;
-      s_lsetot[rr] = (mx + __log2f(wsum)) * kLn2;
-    }
-    __syncthreads();
-    const int rr = threadIdx.x >> 3;
-    const int r = rbase + rr;
-    if (r >= pp.H) continue;
-    float acc[64];
+  float acc[64];
 #pragma unroll
-    for (int t = 0; t < 64; ++t) acc[t] = 0.f;
-    for (int i = 0; i < ncand; ++i) {
-      const int sl = s_slot[i];
-      if (sl < 0) continue;
-      const float w = s_w[i * 32 + rr];
-      const int64_t e0 = (static_cast<int64_t>(sl) * 128 + r) * 512 + sub * 64;
-      if (f32) {
-        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(pp.ws_o) + e0);
-        float4 f[16];
+  for (int t = 0; t < 64; ++t) acc[t] = 0.f;
+  float m = -INFINITY, wsum = 0.f;
+  for (int c = c_first; c <= c_last; ++c) {
+    const int s0 = pp.ws_bounds[c], s1 = pp.ws_bounds[c + 1];
+    if (s1 <= s0) continue;                               // pair without tiles
+    const int sl = 2 * c + (s0 >= ustart ? 0 : 1);        // its first or its last piece
+    const float l = pp.ws_lse[sl * 128 + r];              // log2 domain
+    const int64_t e0 = (static_cast<int64_t>(sl) * 128 + r) * 512 + sub * 64;
+    float x[64];
+    if (f32) {
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(pp.ws_o) + e0);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) f[q] = src[q];
+      for (int q = 0; q < 16; ++q) {
+        const float4 f = src[q];
+        x[4 * q] = f.x;
+        x[4 * q + 1] = f.y;
+        x[4 * q + 2] = f.z;
+        x[4 * q + 3] = f.w;
+      }
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(pp.ws_o) + e0);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          acc[4 * q] = fmaf(w, f[q].x, acc[4 * q]);
-          acc[4 * q + 1] = fmaf(w, f[q].y, acc[4 * q + 1]);
-          acc[4 * q + 2] = fmaf(w, f[q].z, acc[4 * q + 2]);
-          acc[4 * q + 3] = fmaf(w, f[q].w, acc[4 * q + 3]);
-        }
-      } else {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(pp.ws_o) + e0);
-        uint4 h[8];
+      for (int q = 0; q < 8; ++q) {
+        const uint4 h = src[q];
+        const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) h[q] = src[q];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint32_t hw[4] = {h[q].x, h[q].y, h[q].z, h[q].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 f2 = unpack2(hw[j], pp.part_dtype);
-            acc[8 * q + 2 * j] = fmaf(w, f2.x, acc[8 * q + 2 * j]);
-            acc[8 * q + 2 * j + 1] = fmaf(w, f2.y, acc[8 * q + 2 * j + 1]);
-          }
+        for (int j = 0; j < 4; ++j) {
+          const float2 f2 = unpack2(hw[j], pp.part_dtype);
+          x[8 * q + 2 * j] = f2.x;
+          x[8 * q + 2 * j + 1] = f2.y;
         }
       }
     }
-    const int64_t row = part_row(pp, u / pp.P, u % pp.P, r);
+    if (l > m) {   // a new reference maximum (the first piece: the scale is 0)
+      const float sc = exp2f(m - l);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t v[32];
-#pragma unroll
-      for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(acc[32 * h + t]);
-      store_row32(pp.o_part, row * 512 + sub * 64 + 32 * h, v, 1.f, pp.part_dtype);
+      for (int t = 0; t < 64; ++t) acc[t] *= sc;
+      wsum *= sc;
+      m = l;
     }
-    if (sub == 0) pp.lse_part[row] = s_lsetot[rr];
+    const float w = exp2f(l - m);
+#pragma unroll
+    for (int t = 0; t < 64; ++t) acc[t] = fmaf(w, x[t], acc[t]);
+    wsum += w;
   }
+  const float inv = 1.f / wsum;
+  const int64_t row = part_row(pp, u / pp.P, u % pp.P, r);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t v[32];
+#pragma unroll
+    for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(acc[32 * h + t]);
+    store_row32(pp.o_part, row * 512 + sub * 64 + 32 * h, v, inv, pp.part_dtype);
+  }
+  if (sub == 0) pp.lse_part[row] = (m + __log2f(wsum)) * kLn2;
 }
 
 // ---------------------------------------------------------------- launcher
@@ -1002,7 +983,7 @@ static int launch_partial_t(const CUtensorMap& qlat, const CUtensorMap& qpe, con
 // partial grid drains and waits for it on the device (griddepcontrol).
 int launch_partial_merge(const PartialParams& pp, int clusters, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(clusters, 2, 1);
+  cfg.gridDim = dim3(clusters, 4, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
