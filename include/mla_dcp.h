@@ -129,8 +129,9 @@ enum {
  *   err_flag   device int32 or NULL (see conventions)
  *   workspace  device scratch of at least workspace_bytes, or NULL; needs
  *              no initialisation.  With a workspace the GPU's CTA pairs take
- *              exactly equal shares of all KV tiles whenever whole shards
- *              would leave them uneven; a shard cut between pairs has its
+ *              equal shares of the work (every KV tile, plus half a tile's
+ *              worth per shard piece) whenever whole shards would leave them
+ *              uneven; a shard cut between pairs has its
  *              pieces parked there and merged by their LSEs (as in
  *              mla_lse_combine) into o_part / lse_part by a second kernel on
  *              the same stream.  Without one each pair takes whole shards.
