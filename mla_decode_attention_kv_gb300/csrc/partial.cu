@@ -845,7 +845,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 // CTA needs no shared memory and no barrier, and a launch takes few dependent
 // memory round trips (record, share boundaries, then each piece's LSE and
 // values together).
-__global__ void __launch_bounds__(256) mla_partial_merge_kernel(PartialParams pp) {
+__global__ void __launch_bounds__(256, 2) mla_partial_merge_kernel(PartialParams pp) {
   griddep_wait();   // the partial grid has completed and its writes are visible
   griddep_launch_dependents();
   const int4 rec = pp.ws_units[blockIdx.x];
@@ -866,31 +866,6 @@ __global__ void __launch_bounds__(256) mla_partial_merge_kernel(PartialParams pp
     const int sl = 2 * c + (s0 >= ustart ? 0 : 1);        // its first or its last piece
     const float l = pp.ws_lse[sl * 128 + r];              // log2 domain
     const int64_t e0 = (static_cast<int64_t>(sl) * 128 + r) * 512 + sub * 64;
-    float x[64];
-    if (f32) {
-      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(pp.ws_o) + e0);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float4 f = src[q];
-        x[4 * q] = f.x;
-        x[4 * q + 1] = f.y;
-        x[4 * q + 2] = f.z;
-        x[4 * q + 3] = f.w;
-      }
-    } else {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(pp.ws_o) + e0);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint4 h = src[q];
-        const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f2 = unpack2(hw[j], pp.part_dtype);
-          x[8 * q + 2 * j] = f2.x;
-          x[8 * q + 2 * j + 1] = f2.y;
-        }
-      }
-    }
     if (l > m) {   // a new reference maximum (the first piece: the scale is 0)
       const float sc = exp2f(m - l);
 #pragma unroll
@@ -899,9 +874,41 @@ __global__ void __launch_bounds__(256) mla_partial_merge_kernel(PartialParams pp
       m = l;
     }
     const float w = exp2f(l - m);
-#pragma unroll
-    for (int t = 0; t < 64; ++t) acc[t] = fmaf(w, x[t], acc[t]);
     wsum += w;
+    // the piece's 64 values in two halves (fewer live registers: two CTAs
+    // per SM, so every CTA of a launch is resident at once)
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float x[32];
+      if (f32) {
+        const float4* src =
+            reinterpret_cast<const float4*>(static_cast<const float*>(pp.ws_o) + e0 + 32 * half);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 f = src[q];
+          x[4 * q] = f.x;
+          x[4 * q + 1] = f.y;
+          x[4 * q + 2] = f.z;
+          x[4 * q + 3] = f.w;
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(pp.ws_o) +
+                                                          e0 + 32 * half);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 h = src[q];
+          const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f2 = unpack2(hw[j], pp.part_dtype);
+            x[8 * q + 2 * j] = f2.x;
+            x[8 * q + 2 * j + 1] = f2.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 32; ++t) acc[32 * half + t] = fmaf(w, x[t], acc[32 * half + t]);
+    }
   }
   const float inv = 1.f / wsum;
   const int64_t row = part_row(pp, u / pp.P, u % pp.P, r);
