@@ -978,7 +978,7 @@ static int launch_partial_t(const CUtensorMap& qlat, const CUtensorMap& qpe, con
                             cudaStream_t stream) {
   int max_clusters = 0;
   if (prepare_partial<BF16>(&max_clusters) != 0) return -1;
-  // with a workspace every resident pair takes an equal share of the tiles
+  // with a workspace every resident pair takes a share (equal shares of cost)
   const int clusters = pp.split ? pp.split : std::max(1, std::min(pp.num_units, max_clusters));
   if (clusters > max_clusters) return -1;
   mla_partial_kernel<BF16><<<dim3(2 * clusters), dim3(256), PairSmem::kTotal, stream>>>(
