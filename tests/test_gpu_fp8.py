@@ -196,3 +196,15 @@ def test_fp8_full_size_sampled():
         ref = ref_o[:, :, s]
         assert_out_close(got_o[:, :, s], ref, f"o_part shard {s}",
                          rtol=OUT_RTOL + extra / np.abs(ref).max())
+
+
+def test_fp8_many_short_units_per_pair():
+    """The E4M3-cache kernel over 512 short histories in 16 shards: more units
+    per CTA pair than the pair's table of units holds."""
+    cfg = inputs.DecodeConfig(name="fmu", batch=512, heads=16, q_len=1, num_shards=16,
+                              block_size=16, ragged=(1, 200), kv_scale=2.0 ** -8, seed=142, **F8)
+    dp = DeviceProblem(inputs.make_problem(cfg))
+    o_part, lse_part = dp.partial()
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    _check_split(dp, o_part, lse_part)

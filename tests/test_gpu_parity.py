@@ -376,6 +376,22 @@ def test_shard_split_over_many_pairs(history, q_len, cur):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("workspace", ["default", None])
+def test_many_short_units_per_pair(workspace):
+    """512 short histories in 16 shards of 16 tokens: about 108 units per CTA
+    pair, most of them empty or one tile, more than the pair's shared-memory
+    table of units holds (the rest are looked up as they come), and share
+    boundaries that fall between, inside and at the ends of tiny units.
+    Every partial matches the oracle, with and without a workspace."""
+    cfg = inputs.DecodeConfig(name="mu", batch=512, heads=16, q_len=1, num_shards=16,
+                              block_size=16, ragged=(1, 200), seed=141)
+    dp = DeviceProblem(inputs.make_problem(cfg))
+    o_part, lse_part = dp.partial(workspace=workspace)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    _check_partials(dp, o_part, lse_part)
+
+
 def test_workspace_too_small_is_rejected():
     dp = DeviceProblem(inputs.make_problem(SMALL["tiny"]))
     ws = torch.zeros(1024, dtype=torch.uint8, device=dp.dev)
