@@ -296,21 +296,30 @@ class DeviceWorkload:
 
     def time_device(self, steps, warmup, stream, barrier):
         """(ms of all `steps` steps, mean partial-kernel ms per step), device
-        time by CUDA events on the launching stream."""
+        time by CUDA events on the launching stream.  The steps are timed
+        twice: once as they run (the step time), then again with an event pair
+        around every partial launch (its time, for the roofline).  An event
+        recorded between the merge kernel and the fused V-up breaks the
+        V-up's programmatic dependent launch, so the second loop's steps are
+        a few microseconds slower and do not give the step time."""
         import torch
         for i in range(warmup):
             self.step(i, stream)
         barrier()
-        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(steps)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         e0.record(stream)
         for i in range(steps):
-            self.step(warmup + i, stream, kev[i])
+            self.step(warmup + i, stream)
         e1.record(stream)
         barrier()
         total_ms = e0.elapsed_time(e1)
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        barrier()
+        for i in range(steps):
+            self.step(warmup + i, stream, kev[i])
+        barrier()
         partial_ms = sum(a.elapsed_time(b) for a, b in kev) / steps
         if self.err.item() != 0:
             raise RuntimeError(f"{self.name}: device error {self.err.item()} in the timed region")
@@ -321,8 +330,11 @@ class DeviceWorkload:
         copies its inputs from pinned host memory and its output back.  Two
         sets of device input / output buffers alternate, and the copies run
         on a second stream, so step i's copies overlap the kernels of its
-        neighbours (as a serving loop would run them).  One cudaMemcpyAsync
-        per direction and step; returns (ms, h2d bytes, d2h bytes)."""
+        neighbours (as a serving loop would run them).  Each direction has
+        its own copy stream, so step i + 1's inputs are not queued behind
+        step i's output copy (which waits for step i's kernels).  One
+        cudaMemcpyAsync per direction and step; returns (ms, h2d bytes,
+        d2h bytes)."""
         import torch
         prob, cfg, dev = self.prob, self.cfg, self.dev
         parts = [("q_abs", prob.q_abs.view(np.int16)), ("q_pe", prob.q_pe.view(np.int16)),
@@ -349,7 +361,8 @@ class DeviceWorkload:
             return d_in[k][offs[name]:offs[name] + n].view(like.dtype).view(like.shape)
 
         views = [{name: dview(k, name) for name, _ in parts} for k in range(2)]
-        copy = torch.cuda.Stream(device=dev)
+        h2d = torch.cuda.Stream(device=dev)
+        d2h = torch.cuda.Stream(device=dev)
         ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of buffer k landed
         ev_used = [torch.cuda.Event() for _ in range(2)]    # kernels done with buffer k
         ev_out = [torch.cuda.Event() for _ in range(2)]     # output k copied to the host
@@ -360,10 +373,10 @@ class DeviceWorkload:
         def e2e_step(i):
             k, li = i % 2, i % self.layers
             v = views[k]
-            with torch.cuda.stream(copy):
-                copy.wait_event(ev_used[k])
+            with torch.cuda.stream(h2d):
+                h2d.wait_event(ev_used[k])
                 d_in[k].copy_(h_in, non_blocking=True)
-                ev_in[k].record(copy)
+                ev_in[k].record(h2d)
             stream.wait_event(ev_in[k])
             stream.wait_event(ev_out[k])
             self.api.decode_step(v["q_abs"], v["q_pe"], self.caches[li], v["table"], v["lens"],
@@ -372,17 +385,18 @@ class DeviceWorkload:
                                  out=d_out[k], err_flag=self.err, stream=stream,
                                  kv_scale=self.kv_scale)
             ev_used[k].record(stream)
-            with torch.cuda.stream(copy):
-                copy.wait_event(ev_used[k])
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(ev_used[k])
                 h_out[k].copy_(d_out[k].view(torch.int16), non_blocking=True)
-                ev_out[k].record(copy)
+                ev_out[k].record(d2h)
 
         for i in range(warmup):
             e2e_step(i)
         barrier()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(stream)
-        copy.wait_event(f0)
+        h2d.wait_event(f0)
+        d2h.wait_event(f0)
         for i in range(steps):
             e2e_step(warmup + i)
         stream.wait_event(ev_out[0])
