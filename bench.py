@@ -533,7 +533,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": line_roof,
         "e2e": {"value": round(e2e_tbs, 4), "unit": "TB/s",
                 "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
-                "copies": "double-buffered inputs/outputs, copies on a second stream"},
+                "copies": "double-buffered inputs/outputs, copies on one stream per direction"},
         # per step: partial kernel, its split-shard merge kernel, fused combine + V-up;
         # the same three per step in the e2e leg (which also runs the copies)
         "gpu_launches": 3 * args.steps,
