@@ -911,7 +911,8 @@ __global__ void __launch_bounds__(256, 2) mla_partial_merge_kernel(PartialParams
     }
   }
   const float inv = 1.f / wsum;
-  const int64_t row = part_row(pp, u / pp.P, u % pp.P, r);
+  const int ib = u / pp.P;
+  const int64_t row = part_row(pp, static_cast<int64_t>(ib % pp.B) * pp.q_len + ib / pp.B, u % pp.P, r);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t v[32];

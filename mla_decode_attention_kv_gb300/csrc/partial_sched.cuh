@@ -12,8 +12,13 @@ namespace mla {
 // Token range of one unit.  History shard p of sequence b covers
 // [p*len, min(L, (p+1)*len)), len = bs * ceil(L / (S*bs)) (block-aligned,
 // trailing shards possibly empty).  The CURRENT part covers kv_cur[b, 0..i].
-// Units are numbered u = ((b * q_len + i) * P + p), so the parts of one query
-// token are consecutive and a cluster walking a contiguous range reuses Q.
+// Units are numbered u = ((i * B + b) * P + p): the parts of one query token
+// are consecutive, so a cluster walking a contiguous range reuses Q; and with
+// several query tokens (MTP) the units of token i form the i-th block of the
+// order, so the equal shares give the pairs of each block the same KV ranges at
+// the same time: the second token's stream finds the KV in L2 (measured with
+// two tokens: 306 MB of DRAM reads for 302 MB of cache, against 606 MB with
+// the tokens of one sequence next to each other).
 struct UnitInfo {
   int b, i, p;
   int lo, hi;
@@ -28,9 +33,9 @@ template <int TILE>
 __device__ __noinline__ UnitInfo unit_info(const PartialParams& pp, int u) {
   UnitInfo ui;
   ui.p = u % pp.P;
-  const int bi = u / pp.P;
-  ui.i = bi % pp.q_len;
-  ui.b = bi / pp.q_len;
+  const int ib = u / pp.P;   // units by query token, then sequence, then part
+  ui.b = ib % pp.B;
+  ui.i = ib / pp.B;
   ui.current = pp.has_cur && ui.p == pp.S;
   if (ui.current) {
     ui.lo = 0;
