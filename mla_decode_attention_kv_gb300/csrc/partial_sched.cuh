@@ -206,6 +206,13 @@ __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid
   __shared__ int s_load[256];
   __shared__ int s_rng[4];
   __shared__ int s_bound[257];
+  // each unit's tile count, written by the thread that owns the unit in the
+  // first pass and read back by it in the later ones (a unit lookup is a
+  // chain of integer divisions: recomputed in every pass, it made the
+  // partition 7 us long at the start of every launch with one unit per
+  // thread, 14 us with four)
+  constexpr int kNtCache = 2048;
+  __shared__ int s_nt[kNtCache];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   sh.total = 0;
@@ -218,9 +225,12 @@ __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid
   int cnt = 0, cost = 0;   // tiles and cost of this thread's units
   for (int u = a; u < e; ++u) {
     const int nt = unit_info<TILE>(pp, u).ntiles;
+    if (u < kNtCache) s_nt[u] = nt;
     cnt += nt;
     cost += nt > 0 ? kCostPerTile * nt + kCostPerUnit : 0;
   }
+  // this thread's own entries only: no barrier needed before reading them
+  auto unit_tiles = [&](int u) { return u < kNtCache ? s_nt[u] : unit_info<TILE>(pp, u).ntiles; };
   // exclusive block scan of (cost, tiles), packed in one 64-bit word (both
   // sums stay below 2^32): warp inclusive scans, then the warp totals
   const unsigned long long mine = (static_cast<unsigned long long>(cost) << 32) | static_cast<unsigned>(cnt);
@@ -259,7 +269,7 @@ __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid
   if (all_cost > 0) {
     int64_t trun = my_start, crun = my_cstart;
     for (int u = a; u < e; ++u) {
-      const int nt = unit_info<TILE>(pp, u).ntiles;
+      const int nt = unit_tiles(u);
       if (nt == 0) continue;
       const int64_t cend = crun + kCostPerTile * nt + kCostPerUnit;
       for (int c = max(1, static_cast<int>((crun * ncl + all_cost - 1) / all_cost)); c < ncl; ++c) {
@@ -287,7 +297,7 @@ __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid
     // merge kernel and the extra unit ends cost about that much.
     int64_t run = my_start;
     for (int u = a; u < e; ++u) {
-      const int nt = unit_info<TILE>(pp, u).ntiles;
+      const int nt = unit_tiles(u);
       if (nt > 0) atomicAdd(&s_load[sh.cluster_of(run)], kCostPerTile * nt + kCostPerUnit);
       run += nt;
     }
@@ -302,7 +312,7 @@ __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid
   const int64_t hi = sh.start(cid + 1);
   int64_t run = my_start;
   for (int u = a; u < e; ++u) {
-    const int nt = unit_info<TILE>(pp, u).ntiles;
+    const int nt = unit_tiles(u);
     if (nt > 0 && lo < hi) {
       if (split) {
         if (lo >= run && lo < run + nt) {
@@ -324,7 +334,11 @@ __device__ __forceinline__ void partition_tiles(const PartialParams& pp, int cid
   rng.u_begin = s_rng[0];
   rng.j_begin = s_rng[1];
   rng.u_last = s_rng[2];
-  rng.j_stop = split ? s_rng[3] : (rng.u_last >= 0 ? unit_info<TILE>(pp, rng.u_last).ntiles : 0);
+  // (after the barrier above every thread's entries of s_nt are visible)
+  rng.j_stop = split ? s_rng[3]
+                     : (rng.u_last < 0 ? 0
+                        : rng.u_last < kNtCache ? s_nt[rng.u_last]
+                                                : unit_info<TILE>(pp, rng.u_last).ntiles);
   rng.t_begin = static_cast<int>(lo);
   // the unit table of this range (every thread of the CTA passes here)
   const int ncache = rng.u_begin <= rng.u_last ? min(rng.u_last - rng.u_begin + 1, kUnitCache) : 0;
