@@ -131,10 +131,10 @@ enum {
  *              no initialisation.  With a workspace the GPU's CTA pairs take
  *              equal shares of the work (every KV tile, plus half a tile's
  *              worth per shard piece) whenever whole shards would leave them
- *              uneven; a shard cut between pairs has its
- *              pieces parked there and merged by their LSEs (as in
- *              mla_lse_combine) into o_part / lse_part by a second kernel on
- *              the same stream.  Without one each pair takes whole shards.
+ *              uneven; a shard cut between pairs has its pieces parked there
+ *              and merged by their LSEs (as in mla_lse_combine) into o_part /
+ *              lse_part by a second kernel on the same stream.  Without one
+ *              each pair takes whole shards.
  *              Calls that may overlap in time need separate workspaces.
  *   workspace_bytes  size of workspace; at least
  *              mla_dcp_decode_partial_workspace_size(B, q_len, num_shards,
